@@ -1,0 +1,149 @@
+/*
+ * libkda -- KDA (Kimi Delta Attention) layer forward on GB300 (sm_103a).
+ *
+ * The layer is the gated delta rule with one decay per key channel,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t,            alpha_t = exp(log_alpha_t),
+ *
+ * a running state of fixed size (d_k x d_v per sequence and head) as
+ * described on orkas.ai, "Kimi K3 architecture" (German edition), section
+ * "Sequenz: Drei Viertel der Schichten lesen nicht mehr alles".  The decay
+ * is bounded below, log_alpha in [-5, 0] (each step keeps at least 0.67 % of
+ * the state), so the cumulative log-decay over a 16-token tile stays in
+ * [-80, 0] and its reciprocal below e^80; same page, section "Eine
+ * Untergrenze, die einen GPU-Codepfad beseitigte".  That bound is what lets
+ * the chunked kernels evaluate the diagonal tiles with the same dense bf16
+ * tensor-core products as every other tile.
+ *
+ * Conventions for every entry point
+ *   - All pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory.
+ *   - Calls are asynchronous on `stream`; buffers must stay valid until the
+ *     stream reaches the call.  Argument errors are returned synchronously,
+ *     before anything is launched; nothing is printed and no C++ exception
+ *     crosses this interface.
+ *   - Layouts are row-major with the last dimension contiguous.  Activations
+ *     are token-major [B, T, H, d]; states are [B or N, H, d_k, d_v] fp32.
+ *   - q and k are used as given (the caller L2-normalises them).
+ *   - log_alpha must lie in [-5, 0].  With KDA_CHECK_DECAY set in the
+ *     environment (read once per process) the prefill entry points also
+ *     scan it on the device and report a violation through
+ *     kda_last_device_status(); without it, out-of-range values give
+ *     unspecified results.
+ *   - Supported head dims: d_k = d_v = 128, and d_k = d_v = 64 (prefill
+ *     only).  Others return KDA_ERR_UNSUPPORTED.
+ *   - All base pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT).
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifndef KDA_API
+#define KDA_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad cu_seqlens on host */
+    KDA_ERR_UNSUPPORTED = 2, /* head dim or dtype this build does not implement   */
+    KDA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned                  */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
+    KDA_ERR_DECAY_BOUND = 5, /* device found log_alpha outside [-5, 0]            */
+    KDA_ERR_TIMEOUT = 6,     /* a device-side wait hit its iteration limit        */
+    KDA_ERR_WORKSPACE = 7    /* workspace missing or smaller than required        */
+} kda_status_t;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
+
+/*
+ * kda_chunk_fwd -- chunked prefill of B fixed-length sequences.
+ *   q, k, log_alpha : [B, T, H, d_k] bf16
+ *   v               : [B, T, H, d_v] bf16
+ *   beta            : [B, T, H] bf16
+ *   initial_state   : [B, H, d_k, d_v] fp32, or NULL for zeros
+ *   out             : [B, T, H, d_v] in out_dtype (KDA_BF16 or KDA_F32)
+ *   final_state     : [B, H, d_k, d_v] fp32, or NULL (not written); may be
+ *                     the same buffer as initial_state (each state is read
+ *                     once before it is overwritten)
+ *   scale           : multiplies every output (1.0 for the plain layer)
+ *   workspace       : device scratch of kda_chunk_fwd_workspace_size() bytes
+ *                     (may be NULL when that size is 0)
+ * The chunked evaluation (64-token chunks of four 16-token tiles) follows
+ * the blockwise computation the orkas.ai page describes in section "Eine
+ * Untergrenze, die einen GPU-Codepfad beseitigte".  out must not alias any
+ * input.  T may be any value >= 0 (a partial last chunk is masked).
+ */
+KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta,
+                           const float* initial_state, void* out,
+                           kda_dtype_t out_dtype, float* final_state, int B,
+                           int T, int H, int d_k, int d_v, float scale,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* Bytes of device workspace kda_chunk_fwd needs for this shape. */
+KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
+/*
+ * kda_varlen_fwd -- chunked prefill of N packed sequences of unequal length.
+ *   q, k, log_alpha : [T_total, H, d_k] bf16 (a leading batch of 1 is implied)
+ *   v               : [T_total, H, d_v] bf16;   beta : [T_total, H] bf16
+ *   cu_seqlens      : DEVICE int32 [N + 1], non-decreasing, cu[0] = 0,
+ *                     cu[N] = T_total; sequence n owns tokens cu[n]..cu[n+1]-1
+ *   max_seqlen      : an upper bound on the longest sequence (sizes the grid)
+ *   initial_state   : [N, H, d_k, d_v] fp32 or NULL;  final_state likewise
+ *   out             : [T_total, H, d_v]
+ * Chunks start at each sequence's first token; a sequence's last chunk is
+ * masked at its end, so no state leaks between sequences.  The grid is
+ * planned on the device from cu_seqlens; the call does not synchronise.
+ */
+KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
+                            const void* log_alpha, const void* beta,
+                            const int* cu_seqlens, int N, int T_total,
+                            int max_seqlen, const float* initial_state,
+                            void* out, kda_dtype_t out_dtype,
+                            float* final_state, int H, int d_k, int d_v,
+                            float scale, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+KDA_API size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v);
+
+/*
+ * kda_decode_step -- one new token for each of N sequences, state updated IN
+ * PLACE (the orkas.ai page, section "Die Rechnung landet in der
+ * Bereitstellungsinfrastruktur": the state is updated directly and serially).
+ *   q, k, log_alpha : [N, H, d_k] bf16;  v : [N, H, d_v] bf16;  beta : [N, H] bf16
+ *   state           : [N, H, d_k, d_v] fp32, read and overwritten
+ *   out             : [N, H, d_v] in out_dtype
+ * d_k = d_v = 128 only.  One read and one write of the state per call.
+ */
+KDA_API kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
+                             const void* log_alpha, const void* beta,
+                             float* state, void* out, kda_dtype_t out_dtype,
+                             int N, int H, int d_k, int d_v, float scale,
+                             cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+KDA_API const char* kda_status_string(kda_status_t status);
+
+/*
+ * Reads and clears the device status word that kernels set on a decay-bound
+ * violation (when checking is on) or on a wait that hit its iteration limit.
+ * Synchronises `stream`.  Returns KDA_OK when nothing was flagged.
+ */
+KDA_API kda_status_t kda_last_device_status(cudaStream_t stream);
+
+/* Library version string, e.g. "kda-gb300 1.0 sm_103a". */
+KDA_API const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H */

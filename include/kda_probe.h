@@ -1,0 +1,50 @@
+/*
+ * libkda_probe -- TEST-ONLY probes of the tcgen05 / TMA building blocks the
+ * KDA kernels are made of.  Not part of the product interface (kda.h); the
+ * test-suite uses them to check operand layouts, instruction descriptors and
+ * the TMEM lane mapping against a host matmul.  There is no counterpart on
+ * the pages: these exist only to validate this implementation.
+ */
+#ifndef KDA_PROBE_H
+#define KDA_PROBE_H
+
+#include <cuda_runtime_api.h>
+
+#ifndef KDA_API
+#define KDA_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One CTA computes D = (+/-) n_accum * A * B[b_row0 : b_row0 + N]^T with
+ * tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) over K in 16-wide steps.
+ *   A : device bf16 [M][K] row-major (M = 64 or 128)
+ *   B : device bf16 [NB][K] row-major, NB >= b_row0 + N, NB <= 256
+ *   D : device fp32 [128][N] -- the raw accumulator, TMEM lane by column
+ * Operands are placed in shared memory K-major (x_mn = 0) or MN-major
+ * (x_mn = 1) with swizzle code x_sw (2 = 128B, 4 = 64B, 6 = 32B); for
+ * MN-major, x_mn_blocks_contig selects which of the two strides is dense.
+ * status : device int, set to 6 when the completion wait times out.
+ * Returns 0 on launch, 1 on bad arguments, 4 on a CUDA error.
+ */
+KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N, int K, int NB,
+                   int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
+                   int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum, int* status,
+                   cudaStream_t stream);
+
+/*
+ * TMA-loads the 64-token x d-channel tile of head h starting at token t0
+ * from src (bf16 [T][H][d]) in 64-channel boxes with 128-byte swizzle, and
+ * reads it back through the K-major layout function into out (bf16 [64][d]).
+ * Tokens past T read as zero.  Returns 0 / 1 / 4 as above.
+ */
+KDA_API int kda_probe_tma(const void* src, void* out, int T, int H, int d, int h, int t0, int* status,
+                  cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

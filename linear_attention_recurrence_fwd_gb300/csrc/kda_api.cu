@@ -1,0 +1,125 @@
+// C-ABI boundary of libkda: argument validation, status codes and dispatch
+// to the kernels.  No allocation, no printing, no exception crosses it.
+#include <cstdint>
+#include <cstdlib>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool check_decay_env() {
+  static int cached = -1;
+  if (cached < 0) {
+    const char* e = std::getenv("KDA_CHECK_DECAY");
+    cached = (e && e[0] && e[0] != '0') ? 1 : 0;
+  }
+  return cached == 1;
+}
+
+kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+kda_status_t validate_prefill(const void* q, const void* k, const void* v, const void* la,
+                              const void* beta, const float* s0, const void* out,
+                              kda_dtype_t out_dtype, const float* s1, int H, int dk, int dv,
+                              bool has_tokens) {
+  // token tensors may be empty (null) when there are no tokens at all
+  if (has_tokens && (!q || !k || !v || !la || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (dk != dv || !(dk == 128 || dk == 64)) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(la) || !aligned16(beta) ||
+      !aligned16(out) || (s0 && !aligned16(s0)) || (s1 && !aligned16(s1)))
+    return KDA_ERR_ALIGNMENT;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status_t s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_DECAY_BOUND: return "log_alpha outside [-5, 0]";
+    case KDA_ERR_TIMEOUT: return "device wait timed out";
+    case KDA_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* kda_version(void) { return "kda-gb300 1.0 sm_103a"; }
+
+size_t kda_chunk_fwd_workspace_size(int, int, int, int, int) { return 0; }
+size_t kda_varlen_fwd_workspace_size(int, int, int, int, int) { return 0; }
+
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const void* log_alpha,
+                           const void* beta, const float* initial_state, void* out,
+                           kda_dtype_t out_dtype, float* final_state, int B, int T, int H,
+                           int d_k, int d_v, float scale, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
+                                     final_state, H, d_k, d_v, (long long)B * T > 0);
+  if (st != KDA_OK) return st;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env()};
+  return from_cuda(kda::launch_chunk_fwd(p, stream));
+}
+
+kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const void* log_alpha,
+                            const void* beta, const int* cu_seqlens, int N, int T_total,
+                            int max_seqlen, const float* initial_state, void* out,
+                            kda_dtype_t out_dtype, float* final_state, int H, int d_k, int d_v,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!cu_seqlens || N < 0 || T_total < 0 || max_seqlen < 0) return KDA_ERR_INVALID_ARG;
+  if (N > 0 && max_seqlen == 0 && T_total > 0) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(cu_seqlens)) return KDA_ERR_ALIGNMENT;
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
+                                     final_state, H, d_k, d_v, T_total > 0);
+  if (st != KDA_OK) return st;
+  if (N == 0) return KDA_OK;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, cu_seqlens, N, max_seqlen, T_total, H, d_k, scale,
+                      check_decay_env()};
+  return from_cuda(kda::launch_chunk_fwd(p, stream));
+}
+
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* log_alpha,
+                             const void* beta, float* state, void* out, kda_dtype_t out_dtype,
+                             int N, int H, int d_k, int d_v, float scale, cudaStream_t stream) {
+  if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !k || !v || !log_alpha || !beta || !state || !out))
+    return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (d_k != 128 || d_v != 128) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+      !aligned16(state) || !aligned16(out))
+    return KDA_ERR_ALIGNMENT;
+  if ((long long)N * H > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  return from_cuda(kda::launch_decode_step(q, k, v, log_alpha, beta, state, out,
+                                           out_dtype == KDA_F32, N, H, scale, stream));
+}
+
+kda_status_t kda_last_device_status(cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  const int s = kda::read_and_clear_chunk_status(stream, &e);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+  return static_cast<kda_status_t>(s);
+}
+
+}  // extern "C"

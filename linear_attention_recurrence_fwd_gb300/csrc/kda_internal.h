@@ -1,0 +1,40 @@
+// Internal declarations shared by the host API and the kernel translation
+// units of libkda.  Not installed; the public interface is include/kda.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime_api.h>
+
+namespace kda {
+
+__device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
+                               const void* log_alpha, const void* beta, float* state, void* out,
+                               bool out_f32, int N, int H, float scale, cudaStream_t stream);
+
+// Chunked prefill over either B fixed-length sequences (cu_seqlens == null,
+// every sequence T tokens, tensors [B,T,H,d]) or N packed sequences
+// (cu_seqlens on the device, tensors [T_total,H,d]).
+struct ChunkProblem {
+  const void *q, *k, *v, *log_alpha, *beta;
+  const float* initial_state;
+  void* out;
+  bool out_f32;
+  float* final_state;
+  const int* cu_seqlens;  // device, or null
+  int n_seq;              // B or N
+  int T;                  // tokens per sequence (fixed) or max_seqlen (packed)
+  int T_total;            // rows of the token-major tensors
+  int H, d;
+  float scale;
+  bool check_decay;
+};
+
+cudaError_t launch_chunk_fwd(const ChunkProblem& p, cudaStream_t stream);
+
+// Device status word of the chunk kernels (0 = ok, else a kda_status_t).
+int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err);
+
+}  // namespace kda

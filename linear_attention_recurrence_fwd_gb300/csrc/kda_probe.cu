@@ -1,0 +1,184 @@
+// Test-only probes of the building blocks in umma.cuh.  They run one
+// tcgen05.mma sequence, or one TMA tile load, on operands placed in shared
+// memory by the same layout functions the KDA kernels use, and hand the raw
+// result back so a test can compare it with a host matmul / slice.  Not part
+// of the product library (built into libkda_probe.so).
+#include <cuda_runtime.h>
+
+#include "../../include/kda_probe.h"
+#include "tma_host.h"
+#include "umma.cuh"
+
+using namespace kda;
+
+namespace {
+
+struct ProbeArgs {
+  int M, N, K, NB;
+  int a_mn, a_sw, a_mn_blocks_contig;
+  int b_mn, b_sw, b_mn_blocks_contig;
+  int b_row0, neg_a, n_accum;
+};
+
+constexpr int kProbeSmem = 1024 + 32 * 1024 + 64 * 1024 + 1024;
+
+__host__ __device__ OperandLayout probe_layout(uint32_t base, int rows, int K, int mn, int sw,
+                                               int blocks_contig) {
+  OperandLayout L;
+  L.base = base;
+  L.sw = (uint32_t)sw;
+  L.mn_major = mn != 0;
+  const uint32_t S = swizzle_bytes(L.sw);
+  const uint32_t W = S / 2;
+  if (!L.mn_major) {
+    L.sbo = 8 * S;
+    L.kb_stride = (uint32_t)rows * S;
+    L.lbo = 0;
+  } else if (!blocks_contig) {  // the K groups of one MN block are contiguous
+    L.sbo = 8 * S;
+    L.lbo = (uint32_t)K * S;
+    L.kb_stride = 0;
+  } else {  // the MN blocks of one K group are contiguous
+    L.lbo = 8 * S;
+    L.sbo = ((uint32_t)rows / W) * 8 * S;
+    L.kb_stride = 0;
+  }
+  return L;
+}
+
+__global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __restrict__ A,
+                                                         const __nv_bfloat16* __restrict__ B,
+                                                         float* __restrict__ D, ProbeArgs p,
+                                                         int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base_s;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t a_base = (raw + 1023u) & ~1023u;
+  const uint32_t b_base = a_base + 32 * 1024;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  const OperandLayout LA = probe_layout(a_base, p.M, p.K, p.a_mn, p.a_sw, p.a_mn_blocks_contig);
+  const OperandLayout LB = probe_layout(b_base, p.NB, p.K, p.b_mn, p.b_sw, p.b_mn_blocks_contig);
+  // zero both regions, then scatter the logical matrices into them
+  for (uint32_t off = tid * 16; off < 96 * 1024; off += 128 * 16) st_shared_v4(a_base + off, 0, 0, 0, 0);
+  __syncthreads();
+  for (int idx = tid; idx < p.M * p.K; idx += 128) {
+    const int r = idx / p.K, k = idx % p.K;
+    st_shared_u16(layout_addr(LA, r, k), __bfloat16_as_ushort(A[idx]));
+  }
+  for (int idx = tid; idx < p.NB * p.K; idx += 128) {
+    const int r = idx / p.K, k = idx % p.K;
+    st_shared_u16(layout_addr(LB, r, k), __bfloat16_as_ushort(B[idx]));
+  }
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_s, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = tmem_base_s;
+
+  if (tid == 0) {
+    const uint32_t idesc = make_idesc_bf16(p.M, p.N, p.a_mn != 0, p.b_mn != 0, p.neg_a != 0);
+    for (int rep = 0; rep < p.n_accum; ++rep)
+      for (int k0 = 0; k0 < p.K; k0 += 16)
+        umma_bf16(tbase, layout_desc(LA, 0, k0), layout_desc(LB, p.b_row0, k0), idesc,
+                  (rep > 0 || k0 > 0) ? 1u : 0u);
+    umma_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0);
+  if (!ok && lane == 0) atomicExch(status, 6);
+  tc_fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < p.N; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_addr(tbase, 32 * warp, c0), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) D[(size_t)(32 * warp + lane) * p.N + c0 + i] = v[i];
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+__global__ void __launch_bounds__(128) probe_tma_kernel(const __grid_constant__ CUtensorMap map,
+                                                        __nv_bfloat16* __restrict__ out, int d,
+                                                        int h, int t0, int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint64_t bar;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const int nblk = d / 64;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)nblk * 64 * 64 * 2);
+    for (int b = 0; b < nblk; ++b)
+      tma_load_3d(base_ptr + b * 8192, &map, &bar, b * 64, h, t0);
+  }
+  if (!mbar_wait(&bar, 0)) {
+    if (threadIdx.x == 0) atomicExch(status, 6);
+    return;
+  }
+  // read back through the K-major SW128 layout: row = token, k = channel
+  OperandLayout L;
+  L.base = base;
+  L.sw = SW_128;
+  L.mn_major = false;
+  L.sbo = 1024;
+  L.kb_stride = 8192;
+  L.lbo = 0;
+  for (int idx = threadIdx.x; idx < 64 * d; idx += blockDim.x) {
+    const int r = idx / d, c = idx % d;
+    out[idx] = __ushort_as_bfloat16(ld_shared_u16(layout_addr(L, r, c)));
+  }
+}
+
+}  // namespace
+
+extern "C" KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N, int K, int NB,
+                              int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
+                              int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum,
+                              int* status, cudaStream_t stream) {
+  if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K % 16 || K > 128 || K < 16)
+    return 1;
+  if (NB < b_row0 + N || NB > 256 || (a_mn && M % 64) || n_accum < 1) return 1;
+  ProbeArgs p{M, N, K, NB, a_mn, a_sw, a_mn_blocks_contig, b_mn, b_sw, b_mn_blocks_contig,
+              b_row0, neg_a, n_accum};
+  if (cudaFuncSetAttribute(probe_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kProbeSmem) != cudaSuccess)
+    return 4;
+  probe_umma_kernel<<<1, 128, kProbeSmem, stream>>>(static_cast<const __nv_bfloat16*>(A),
+                                                    static_cast<const __nv_bfloat16*>(B), D, p,
+                                                    status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+extern "C" KDA_API int kda_probe_tma(const void* src, void* out, int T, int H, int d, int h, int t0,
+                             int* status, cudaStream_t stream) {
+  if (!(d == 64 || d == 128) || h < 0 || h >= H) return 1;
+  CUtensorMap map;
+  if (!make_map_3d_bf16(&map, src, (uint64_t)d, (uint64_t)H, (uint64_t)T, (uint64_t)d,
+                        (uint64_t)H * d, 64, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return 4;
+  const int smem = 1024 + 16384;
+  if (cudaFuncSetAttribute(probe_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return 4;
+  probe_tma_kernel<<<1, 128, smem, stream>>>(map, static_cast<__nv_bfloat16*>(out), d, h, t0,
+                                             status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}

@@ -1,0 +1,102 @@
+"""GPU probes of the tcgen05 / TMA building blocks: operand layouts,
+descriptors, the instruction descriptor and the TMEM lane mapping, checked
+against a host fp64 matmul (and a host slice for TMA)."""
+import ctypes
+
+import pytest
+import torch
+
+from linear_attention_recurrence_fwd_gb300 import binding, build
+
+pytestmark = pytest.mark.gpu
+
+SW128, SW64, SW32 = 2, 4, 6
+
+
+@pytest.fixture(scope="module")
+def probe(cuda_device):
+    build.build()
+    return binding.load_probe()
+
+
+def _run(probe, M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0=0, NB=None, neg=0, acc=1,
+         seed=0):
+    NB = NB or (b_row0 + N)
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(M, K, generator=g).bfloat16()
+    B = torch.randn(NB, K, generator=g).bfloat16()
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.kda_probe_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, NB, a_mn, a_sw,
+                              a_bc, b_mn, b_sw, b_bc, b_row0, neg, acc, st.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0, "MMA completion wait timed out"
+    exp = (A.double() @ B[b_row0:b_row0 + N].double().T) * acc * (-1.0 if neg else 1.0)
+    return D.cpu().double(), exp
+
+
+def _close(a, b):
+    return torch.allclose(a, b, rtol=1e-3, atol=1e-3)
+
+
+CASES = [
+    # M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0, NB
+    (128, 64, 128, 0, SW128, 0, 0, SW128, 0, 0, None),
+    (128, 256, 64, 0, SW128, 0, 0, SW128, 0, 0, None),
+    (128, 64, 128, 1, SW128, 0, 0, SW128, 0, 0, None),
+    (128, 64, 128, 1, SW128, 1, 0, SW128, 0, 0, None),
+    (128, 64, 128, 0, SW128, 0, 1, SW128, 0, 0, None),
+    (128, 128, 64, 0, SW128, 0, 1, SW128, 1, 0, None),
+    (128, 128, 64, 0, SW128, 0, 1, SW128, 0, 0, None),
+    (128, 16, 128, 0, SW128, 0, 1, SW128, 0, 16, 64),
+    (128, 16, 128, 0, SW128, 0, 1, SW128, 0, 48, 64),
+    (128, 32, 64, 0, SW128, 0, 1, SW128, 0, 32, 64),
+    (128, 16, 128, 0, SW128, 0, 1, SW32, 0, 0, None),
+    (128, 16, 128, 0, SW128, 0, 1, SW32, 0, 16, 32),
+    (128, 32, 64, 0, SW64, 0, 0, SW64, 0, 0, None),
+    (128, 32, 64, 1, SW64, 0, 1, SW64, 0, 0, None),
+    (128, 64, 64, 0, SW128, 0, 0, SW128, 0, 16, 128),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_umma_m128_layouts(probe, case):
+    M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0, NB = case
+    D, exp = _run(probe, M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0, NB)
+    assert _close(D, exp), f"max err {(D - exp).abs().max().item():.3e}"
+
+
+def test_umma_negate_and_accumulate(probe):
+    D, exp = _run(probe, 128, 64, 64, 0, SW128, 0, 1, SW128, 0, neg=1, acc=3)
+    assert _close(D, exp)
+
+
+def test_umma_m64_lane_mapping(probe):
+    """Where the 64 rows of an M=64 accumulator land among the 128 TMEM lanes."""
+    D, exp = _run(probe, 64, 32, 64, 0, SW128, 0, 0, SW128, 0)
+    found = {}
+    for m in range(64):
+        lanes = [l for l in range(128) if torch.allclose(D[l], exp[m], rtol=1e-3, atol=1e-3)]
+        found[m] = lanes
+    expected = {m: [32 * (m // 16) + m % 16] for m in range(64)}
+    assert found == expected, f"lane mapping: {found}"
+
+
+@pytest.mark.parametrize("d,t0", [(128, 0), (128, 64), (64, 32)])
+def test_tma_tile_matches_layout(probe, d, t0):
+    T, H, h = 100, 3, 1
+    src = torch.randn(T, H, d).bfloat16().cuda()
+    out = torch.full((64, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.kda_probe_tma(src.data_ptr(), out.data_ptr(), T, H, d, h, t0, st.data_ptr(),
+                             torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    exp = torch.zeros(64, d, dtype=torch.bfloat16)
+    n = min(64, T - t0)
+    exp[:n] = src[t0:t0 + n, h].cpu()
+    assert torch.equal(out.cpu(), exp)
