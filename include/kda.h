@@ -33,7 +33,8 @@
  *     unspecified results.
  *   - Supported head dims: d_k = d_v = 128, and d_k = d_v = 64 (prefill
  *     only).  Others return KDA_ERR_UNSUPPORTED.
- *   - All base pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT).
+ *   - Base pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT), except
+ *     beta, which needs only its natural 2-byte alignment.
  */
 #ifndef KDA_H
 #define KDA_H

@@ -112,7 +112,7 @@ def _need(t, dtype, name):
 
 
 def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
-                  out_dtype=torch.bfloat16, output_final_state=True, out=None,
+                  out_dtype=torch.float32, output_final_state=True, out=None,
                   final_state=None, stream=None):
     """Chunked prefill.  q,k,log_alpha [B,T,H,dk] bf16; v [B,T,H,dv] bf16;
     beta [B,T,H] bf16; initial_state [B,H,dk,dv] fp32 or None.
@@ -137,7 +137,7 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
 
 
 def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, max_seqlen, initial_state=None,
-                   scale=1.0, out_dtype=torch.bfloat16, output_final_state=True, out=None,
+                   scale=1.0, out_dtype=torch.float32, output_final_state=True, out=None,
                    final_state=None, stream=None):
     """Packed prefill.  Tensors [T_total,H,*] (or [1,T_total,H,*]);
     cu_seqlens int32 [N+1] on the device.  Returns (out, final_state [N,H,dk,dv])."""
@@ -163,7 +163,7 @@ def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, max_seqlen, initial_sta
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, state, scale=1.0, out=None,
-                    out_dtype=torch.bfloat16, stream=None):
+                    out_dtype=torch.float32, stream=None):
     """One token per sequence; `state` [N,H,dk,dv] fp32 is updated in place.
     q,k,log_alpha [N,H,dk], v [N,H,dv], beta [N,H] (bf16).  Returns out [N,H,dv]."""
     lib = load()

@@ -9,6 +9,7 @@
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 
 bool check_decay_env() {
   static int cached = -1;
@@ -30,7 +31,8 @@ kda_status_t validate_prefill(const void* q, const void* k, const void* v, const
   if (H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
   if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
   if (dk != dv || !(dk == 128 || dk == 64)) return KDA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(la) || !aligned16(beta) ||
+  // q, k, v, log_alpha are read by TMA (16-byte rule); beta is read per element
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(la) || !aligned2(beta) ||
       !aligned16(out) || (s0 && !aligned16(s0)) || (s1 && !aligned16(s1)))
     return KDA_ERR_ALIGNMENT;
   return KDA_OK;
@@ -107,7 +109,7 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
   if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
   if (d_k != 128 || d_v != 128) return KDA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
-      !aligned16(state) || !aligned16(out))
+      !aligned2(beta) || !aligned16(state) || !aligned16(out))
     return KDA_ERR_ALIGNMENT;
   if ((long long)N * H > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
   if (N == 0) return KDA_OK;

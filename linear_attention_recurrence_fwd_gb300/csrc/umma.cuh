@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace kda {
 
@@ -148,17 +149,23 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
-                                                       bool b_mn_major, bool negate_a = false) {
+// Instruction descriptor for kind::f16 with an fp32 accumulator; A and B
+// are both bf16 (fp16 = false) or both fp16 (fp16 = true).
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                  bool negate_a = false, bool fp16 = false) {
   return (1u << 4)                               // D format: f32
-         | (1u << 7)                             // A format: bf16
-         | (1u << 10)                            // B format: bf16
+         | ((fp16 ? 0u : 1u) << 7)               // A format: 0 = f16, 1 = bf16
+         | ((fp16 ? 0u : 1u) << 10)              // B format
          | ((negate_a ? 1u : 0u) << 13)          // negate A
          | ((a_mn_major ? 1u : 0u) << 15)        // A major: 0 = K, 1 = MN
          | ((b_mn_major ? 1u : 0u) << 16)        // B major
          | ((uint32_t)(N >> 3) << 17)            // N / 8
          | ((uint32_t)(M >> 4) << 24);           // M / 16
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
+                                                       bool b_mn_major, bool negate_a = false) {
+  return make_idesc(M, N, a_mn_major, b_mn_major, negate_a, false);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
@@ -248,6 +255,10 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -40,3 +40,29 @@ def assert_state_close(s, s_ref, rel=STATE_REL, what="state"):
     assert np.isfinite(_np(s)).all(), f"{what}: non-finite values"
     assert e <= rel, f"{what}: ||dS||/||S|| = {e:.3e}"
     return e
+
+
+def assert_bf16_output_close(o, o_ref, max_rel=MAX_REL, mean_rel=MEAN_REL, what="out"):
+    """bf16 outputs: the bar above plus the storage rounding itself, i.e.
+    |o - ref| <= max_rel * rms + 2^-8 |ref| elementwise and
+    mean |o - ref| <= mean_rel * rms + mean(2^-9 |ref|).  A single bf16
+    rounding (relative error up to 2^-9, 2^-8 across a rounding boundary) of
+    an output near 10x the RMS already exceeds max_rel * rms on its own."""
+    o, o_ref = _np(o), _np(o_ref)
+    assert np.isfinite(o).all(), f"{what}: non-finite values"
+    rms = np.sqrt(np.mean(o_ref ** 2))
+    d = np.abs(o - o_ref)
+    excess = d - (max_rel * rms + 2.0 ** -8 * np.abs(o_ref))
+    assert excess.max() <= 0, f"{what}: worst excess {excess.max() / rms:.3e} rms"
+    mean_bound = mean_rel * rms + np.mean(2.0 ** -9 * np.abs(o_ref))
+    assert d.mean() <= mean_bound, f"{what}: mean {d.mean() / rms:.3e} rms"
+
+
+def round_like(ref, out):
+    """The oracle rounded to the output's storage type: for bf16 outputs the
+    final rounding is a precision decision both sides take the same way, so
+    the comparison measures the kernel's arithmetic, not the storage format."""
+    ref = _np(ref)
+    if isinstance(out, torch.Tensor) and out.dtype == torch.bfloat16:
+        return torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    return ref

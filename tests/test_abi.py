@@ -81,6 +81,7 @@ def test_decode_argument_errors(lib):
     assert call(dk=64) == 2
     assert call(dt=3) == 2
     assert call(st=MIS) == 3
+    assert lib.kda_decode_step(F, F, F, F, ctypes.c_void_p(17), F, F, 0, 4, 2, 128, 128, 1.0, None) == 3
 
 
 def test_workspace_sizes_are_queryable(lib):

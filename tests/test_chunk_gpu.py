@@ -1,0 +1,127 @@
+"""Chunked prefill on the GPU (through the C-ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_recurrence_fwd_gb300 import binding, build
+from linear_attention_recurrence_fwd_gb300 import inputs as gen
+from oracle import oracle as orc
+from parity import (assert_bf16_output_close, assert_output_close, assert_state_close,
+                    output_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    build.build()
+
+
+def _to(x, dev="cuda"):
+    return {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+
+
+def _run(x, out_dtype=torch.float32, scale=1.0):
+    g = _to(x)
+    out, fin = binding.kda_chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                     g["initial_state"], scale=scale, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def _ref(x, scale=1.0):
+    return orc.kda_recurrence(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                              x["initial_state"], scale=scale)
+
+
+def test_tiny_workload():
+    """B=1, T=256, H=2, d=64, zero initial state, fp32 output and state."""
+    w = gen.WORKLOADS["tiny"]
+    x = gen.workload_inputs(w)
+    out, fin = _run(x, out_dtype=w.out_dtype)
+    ro, rs = _ref(x)
+    assert_output_close(out, ro)
+    assert_state_close(fin, rs)
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 130, 200])
+def test_ragged_lengths(T):
+    x = gen.make_inputs(1, T, 2, 128, 128, seed=T, init_std=0.02)
+    out, fin = _run(x)
+    ro, rs = _ref(x)
+    assert_output_close(out, ro)
+    assert_state_close(fin, rs)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_batch_and_bf16_output(d):
+    x = gen.make_inputs(3, 100, 3, d, d, seed=5, init_std=0.02)
+    out, fin = _run(x, out_dtype=torch.bfloat16, scale=0.75)
+    ro, rs = _ref(x, scale=0.75)
+    assert out.dtype == torch.bfloat16
+    assert_bf16_output_close(out, ro)
+    assert_state_close(fin, rs)
+
+
+def _stress(kind, T=1024, H=2, seed=9):
+    x = gen.make_inputs(1, T, H, 128, 128, seed=seed, init_std=0.02)
+    la = x["log_alpha"].float()
+    if kind == "slow_decay":      # state lives across many chunks
+        la = (la * 0.01)
+    elif kind == "at_bound":      # every step at the bound: tile sums exactly -80
+        la = torch.full_like(la, -5.0)
+    elif kind == "channel_mix":   # half the channels ~0, half ~-5
+        la[..., :64] = -0.001
+        la[..., 64:] = -4.999
+    elif kind == "beta_one":
+        x["beta"] = torch.ones_like(x["beta"])
+    x["log_alpha"] = la.to(torch.bfloat16)
+    return x
+
+
+@pytest.mark.parametrize("kind", ["slow_decay", "at_bound", "channel_mix", "beta_one"])
+def test_stress_inputs(kind):
+    x = _stress(kind)
+    assert x["log_alpha"].float().min() >= -5.0
+    out, fin = _run(x)
+    ro, rs = _ref(x)
+    assert_output_close(out, ro, what=kind)
+    assert_state_close(fin, rs, what=kind)
+
+
+def test_split_and_resume_on_gpu():
+    """run(0:T) == run(T1:T) started from run(0:T1).final, T1 aligned or not."""
+    x = gen.make_inputs(1, 300, 2, 128, 128, seed=21, init_std=0.02)
+    ro, rs = _ref(x)
+    for T1 in (64, 100):
+        a = {k: (v[:, :T1].contiguous() if k != "initial_state" else v) for k, v in x.items()}
+        b = {k: (v[:, T1:].contiguous() if k != "initial_state" else None) for k, v in x.items()}
+        oa, fa = _run(a)
+        b["initial_state"] = fa.cpu()
+        ob, fb = _run(b)
+        assert_output_close(torch.cat([oa, ob], 1), ro, what=f"T1={T1}")
+        assert_state_close(fb, rs)
+
+
+def test_in_place_state_and_empty_sequence():
+    x = gen.make_inputs(1, 77, 2, 128, 128, seed=22, init_std=0.02)
+    g = _to(x)
+    s = g["initial_state"].clone()
+    out, fin = binding.kda_chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], s,
+                                     out_dtype=torch.float32, final_state=s)
+    torch.cuda.synchronize()
+    ro, rs = _ref(x)
+    assert_state_close(s, rs)
+    e = {k: (v[:, :0].contiguous() if k != "initial_state" else v) for k, v in x.items()}
+    _, f0 = _run(e)
+    assert torch.equal(f0.cpu(), x["initial_state"])
+
+
+def test_prefill_8k_workload_all_outputs():
+    """B=1, T=8192, H=32, d=128, random initial state; every output compared."""
+    w = gen.WORKLOADS["prefill_8k"]
+    x = gen.workload_inputs(w)
+    out, fin = _run(x)
+    ro, rs = _ref(x)
+    assert_output_close(out, ro)
+    assert_state_close(fin, rs)

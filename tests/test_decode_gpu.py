@@ -6,7 +6,8 @@ import torch
 from linear_attention_recurrence_fwd_gb300 import binding, build
 from linear_attention_recurrence_fwd_gb300 import inputs as gen
 from oracle import oracle as orc
-from parity import assert_output_close, assert_state_close
+from parity import (assert_bf16_output_close, assert_output_close, assert_state_close,
+                    output_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +36,10 @@ def test_decode_one_step(out_dtype):
                                 out_dtype=out_dtype)
     torch.cuda.synchronize()
     ro, rs = orc.decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["state"])
-    tol = (1e-5, 1e-6) if out_dtype == torch.float32 else (2e-2, 2e-3)
-    assert_output_close(o, ro, *tol)
+    if out_dtype == torch.float32:
+        assert_output_close(o, ro, 1e-5, 1e-6)
+    else:
+        assert_bf16_output_close(o, ro)
     assert_state_close(d["state"], rs, 1e-6)
 
 
@@ -56,15 +59,22 @@ def test_decode_chained_steps_and_scale():
     assert_state_close(dstate, ref_state, 1e-5)
 
 
-def test_decode_full_size_step():
-    """256 sequences x 32 heads (the decode workload), one step, every output."""
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_decode_full_size_step(out_dtype):
+    """256 sequences x 32 heads (the decode workload), one step, every output.
+    bf16 outputs get the storage-rounding allowance: decode outputs have tails
+    near 20x their RMS, where bf16's own rounding alone exceeds the max bar."""
     w = gen.WORKLOADS["decode"]
     x = _decode_inputs(w.B, w.H, seed=w.seed)
     d = _gpu(x)
-    o = binding.kda_decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["state"])
+    o = binding.kda_decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["state"],
+                                out_dtype=out_dtype)
     torch.cuda.synchronize()
     ro, rs = orc.decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["state"])
-    assert_output_close(o, ro)
+    if out_dtype == torch.float32:
+        assert_output_close(o, ro, 1e-5, 1e-6)
+    else:
+        assert_bf16_output_close(o, ro)
     assert_state_close(d["state"], rs)
 
 
