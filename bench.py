@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""KDA forward benchmark on GB300.
+
+One step = one chunked prefill of the T = 65536, H = 32, d = 128 problem
+(B = 1, random fp32 initial state) through the C-ABI library, inputs resident
+in HBM.  The same run also measures the decode step (256 sequences x 32
+heads, 1000 chained in-place steps) and reports it beside the headline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
+own copy of the problem on its own GPU (independent heads/sequences: no
+collective on the data path), timings are maxed over ranks and `value` is
+the aggregate.  `--impl reference` times the fp64 CPU oracle on the host's
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill Mtok/s & % BF16 tensor peak at T=64k; decode state GB/s % HBM"
+FLOP_PER_TOKEN_HEAD = 2 * (5 * 64 * 128 + 3 * 128 * 128)  # 180224, chunk 64, d 128
+L2_BYTES = 126 * 2 ** 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def prefill_bytes(tokens, H, d, out_bytes, n_states):
+    """Compulsory HBM bytes of one prefill: q, k, v, log_alpha (bf16), beta
+    (bf16), the output, and the fp32 state read and written once."""
+    return tokens * H * (4 * d * 2 + 2 + d * out_bytes) + 2 * n_states * H * d * d * 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kda_clocks_{os.getpid()}.csv")
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = ["-i", str(device_index)]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("kda_chunk.cu", "umma.cuh"):
+        h.update(open(os.path.join(ROOT, "linear_attention_recurrence_fwd_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else null)."""
+    p = os.path.join(ROOT, "profiles", "chunk_prefill_traffic.json")
+    try:
+        d = json.load(open(p))
+        if d.get("kernel_sha") == kernel_hash():
+            return float(d["dram_bytes_per_launch_full_size"])
+    except Exception:
+        pass
+    return None
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def reduce_max(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample(x, heads, threads=0):
+    """Time the fp64 oracle on `heads` heads of the full-length problem."""
+    from oracle import oracle as orc
+
+    sub = {k: x[k][:, :, :heads].cpu() for k in ("q", "k", "v", "log_alpha", "beta")}
+    s0 = x["initial_state"][:, :heads].cpu() if x["initial_state"] is not None else None
+    t0 = time.perf_counter()
+    orc.kda_recurrence(sub["q"], sub["k"], sub["v"], sub["log_alpha"], sub["beta"], s0,
+                       threads=threads)
+    return time.perf_counter() - t0, orc.max_threads()
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores,
+    each step a bounded sample (one head of the T = 65536 problem)."""
+    if rank != 0:
+        return
+    from linear_attention_recurrence_fwd_gb300 import inputs as gen
+
+    w = gen.WORKLOADS["prefill_64k"]
+    x = gen.make_inputs(1, w.T, 1, w.dk, w.dv, w.seed, w.decay_mean, w.init_std)
+    for _ in range(args.warmup):
+        oracle_sample(x, 1)
+    times = []
+    cores = 1
+    for _ in range(args.steps):
+        t, cores = oracle_sample(x, 1)
+        times.append(t)
+    sec = statistics.mean(times)
+    # one head of H: the whole problem's token rate is 1/H of the head rate
+    value = w.T / w.H / sec / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 * w.H, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill_64k: B=1 T=65536 H=32 d=128", "B": 1, "T": w.T,
+                   "H": w.H, "d": w.dk},
+        "cpu_baseline": {"value": value, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"1 of {w.H} heads, all {w.T} tokens, per step"},
+        "e2e": {"value": value, "unit": "Mtok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(local):
+    """Small, fixed case for ncu captures (a few GB on the device at most)."""
+    from linear_attention_recurrence_fwd_gb300 import binding
+    from linear_attention_recurrence_fwd_gb300 import inputs as gen
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = gen.WORKLOADS["prefill_8k"]
+    x = gen.workload_inputs(w, device=dev)
+    a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    out = torch.empty(x["v"].shape, dtype=torch.float32, device=dev)
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.kda_chunk_fwd(*a, x["initial_state"], out=out, final_state=fin)
+    wd = gen.WORKLOADS["decode"]
+    xd = gen.make_inputs(wd.B, 1, wd.H, 128, 128, wd.seed, init_std=wd.init_std, device=dev)
+    d = [xd[k][:, 0].contiguous() for k in ("q", "k", "v", "log_alpha", "beta")]
+    o = torch.empty((wd.B, wd.H, 128), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.kda_decode_step(*d, xd["initial_state"], out=o)
+    torch.cuda.synchronize()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-heads", type=int, default=32)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--case", choices=["bench", "ncu"], default="bench",
+                    help="ncu: only run the small profiling case (3 prefills at T=8192 "
+                         "H=32, then 3 decode steps) and exit")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if args.case == "ncu":
+        run_profile_case(local)
+        return
+
+    from linear_attention_recurrence_fwd_gb300 import binding
+    from linear_attention_recurrence_fwd_gb300 import build as kbuild
+    from linear_attention_recurrence_fwd_gb300 import inputs as gen
+
+    kbuild.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---------------- prefill, T = 65536, H = 32: inputs resident in HBM
+    w = gen.WORKLOADS["prefill_64k"]
+    x = gen.workload_inputs(w, device=dev)
+    args_in = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    out = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev)
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def step():
+        binding.kda_chunk_fwd(*args_in, x["initial_state"], out=out, final_state=fin)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    status = binding.kda_last_device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status}: {binding.kda_status_string(status)}")
+
+    # ---------------- decode: 256 x 32 heads, 1000 chained in-place steps
+    wd = gen.WORKLOADS["decode"]
+    pool = 64
+    xd = gen.make_inputs(wd.B, pool, wd.H, 128, 128, wd.seed, init_std=wd.init_std, device=dev,
+                         n_states=wd.B)
+    dsets = [[xd[k][:, s].contiguous() for k in ("q", "k", "v", "log_alpha", "beta")]
+             for s in range(pool)]
+    dstate = xd["initial_state"]
+    dout = torch.empty((wd.B, wd.H, 128), dtype=torch.float32, device=dev)
+    for s in range(3):
+        binding.kda_decode_step(*dsets[s % pool], dstate, out=dout)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for s in range(args.decode_steps):
+        binding.kda_decode_step(*dsets[s % pool], dstate, out=dout)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    dec_us_local = d0.elapsed_time(d1) * 1e3 / args.decode_steps
+
+    # ---------------- end to end: pinned host inputs -> call -> host output
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hfin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in x.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = hout.numel() * 4 + hfin.numel() * 4
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        binding.kda_chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["log_alpha"], dbuf["beta"],
+                              dbuf["initial_state"], out=out, final_state=fin)
+        hout.copy_(out, non_blocking=True)
+        hfin.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms_local = g0.elapsed_time(g1) / args.e2e_steps
+    del dbuf, host
+
+    ms = reduce_max(ms_local, ws)
+    dec_us = reduce_max(dec_us_local, ws)
+    e2e_ms = reduce_max(e2e_ms_local, ws)
+    tokens = w.B * w.T
+    value = ws * tokens / (ms * 1e-3) / 1e6
+    e2e_value = ws * tokens / (e2e_ms * 1e-3) / 1e6
+
+    if rank != 0:
+        return
+    alg_bytes = prefill_bytes(tokens, w.H, w.dk, 4, w.B)
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    flops = tokens * w.H * FLOP_PER_TOKEN_HEAD
+    tflops = flops / (ms * 1e-3) / 1e12
+    dec_bytes = wd.B * wd.H * (2 * 128 * 128 * 4 + 4 * 128 * 2 + 2 + 128 * 4)
+    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+
+    cpu = None
+    if not args.skip_cpu:
+        sec, cores = oracle_sample(x, args.cpu_heads)
+        cpu = {"value": tokens * args.cpu_heads / w.H / sec / 1e6, "unit": "Mtok/s",
+               "cores": cores, "kind": "oracle",
+               "sample": f"{args.cpu_heads} of {w.H} heads, all {w.T} tokens (fp64, {sec:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill_64k: B=1 T=65536 H=32 d=128, fp32 out, fp32 state",
+                   "B": w.B, "T": w.T, "H": w.H, "d": w.dk, "chunk": 64,
+                   "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.2f} GB per step)",
+                   "parallelism": f"replicas x{ws}"},
+        "tensor": {"tflops": tflops, "frac_burst": tflops / pk["bf16"],
+                   "frac_sustained": tflops / pk["bf16_sus"], "peak_src": pk["src"],
+                   "flop_per_token_head": FLOP_PER_TOKEN_HEAD},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm"], "traffic": recorded_traffic(),
+                     "alg_bytes_per_launch": alg_bytes, "peak_src": pk["src"]},
+        "decode": {"us_per_step": dec_us, "state_gbs": dec_gbs, "hbm_frac": dec_gbs / pk["hbm"],
+                   "steps": args.decode_steps, "workload": "256 seq x 32 heads x d128, fp32 out"},
+        "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

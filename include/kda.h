@@ -74,8 +74,11 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
  *                     the same buffer as initial_state (each state is read
  *                     once before it is overwritten)
  *   scale           : multiplies every output (1.0 for the plain layer)
- *   workspace       : device scratch of kda_chunk_fwd_workspace_size() bytes
- *                     (may be NULL when that size is 0)
+ *   workspace       : device scratch of at least kda_chunk_fwd_workspace_size()
+ *                     bytes, 16-byte aligned, owned by the caller; it holds
+ *                     the per-(chunk, head) intermediate records (65 KiB
+ *                     each) passed from the intra-chunk stage to the state
+ *                     pass.  Too small or NULL -> KDA_ERR_WORKSPACE.
  * The chunked evaluation (64-token chunks of four 16-token tiles) follows
  * the blockwise computation the orkas.ai page describes in section "Eine
  * Untergrenze, die einen GPU-Codepfad beseitigte".  out must not alias any
@@ -89,7 +92,8 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
                            void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
-/* Bytes of device workspace kda_chunk_fwd needs for this shape. */
+/* Bytes of device workspace kda_chunk_fwd needs for this shape:
+ * B * ceil(T / 64) * H * 66560. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /*
@@ -101,9 +105,12 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_
  *   max_seqlen      : an upper bound on the longest sequence (sizes the grid)
  *   initial_state   : [N, H, d_k, d_v] fp32 or NULL;  final_state likewise
  *   out             : [T_total, H, d_v]
+ *   workspace       : at least kda_varlen_fwd_workspace_size() bytes
  * Chunks start at each sequence's first token; a sequence's last chunk is
- * masked at its end, so no state leaks between sequences.  The grid is
- * planned on the device from cu_seqlens; the call does not synchronise.
+ * masked at its end, so no state leaks between sequences.  The chunk list is
+ * planned on the device from cu_seqlens (a prefix sum of ceil(len / 64));
+ * the call does not synchronise.  A negative length flags
+ * KDA_ERR_INVALID_ARG in the device status word.
  */
 KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             const void* log_alpha, const void* beta,
@@ -114,6 +121,7 @@ KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             float scale, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
+/* (T_total / 64 + N) * H * 66560 plus 4 (N + 1) bytes rounded up to 1 KiB. */
 KDA_API size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v);
 
 /*

@@ -27,13 +27,15 @@ extern "C" {
  * Operands are placed in shared memory K-major (x_mn = 0) or MN-major
  * (x_mn = 1) with swizzle code x_sw (2 = 128B, 4 = 64B, 6 = 32B); for
  * MN-major, x_mn_blocks_contig selects which of the two strides is dense.
+ * tf32 = 1 stores both operands as fp32 and runs kind::tf32 (8-wide K steps);
+ * then M*K*4 <= 32 KiB and NB*K*4 <= 64 KiB, and neg_a must be 0.
  * status : device int, set to 6 when the completion wait times out.
  * Returns 0 on launch, 1 on bad arguments, 4 on a CUDA error.
  */
 KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N, int K, int NB,
                    int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
-                   int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum, int* status,
-                   cudaStream_t stream);
+                   int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum, int tf32,
+                   int* status, cudaStream_t stream);
 
 /*
  * TMA-loads the 64-token x d-channel tile of head h starting at token t0

@@ -76,7 +76,7 @@ def load_probe(path: str = PROBE_LIB_PATH):
         if not os.path.exists(path):
             raise RuntimeError(f"libkda_probe.so not found at {path}")
         lib = ctypes.CDLL(path)
-        lib.kda_probe_umma.argtypes = [_vp, _vp, _vp] + [_i] * 13 + [_vp, _vp]
+        lib.kda_probe_umma.argtypes = [_vp, _vp, _vp] + [_i] * 14 + [_vp, _vp]
         lib.kda_probe_umma.restype = _i
         lib.kda_probe_tma.argtypes = [_vp, _vp] + [_i] * 5 + [_vp, _vp]
         lib.kda_probe_tma.restype = _i

@@ -58,25 +58,36 @@ const char* kda_status_string(kda_status_t s) {
 
 const char* kda_version(void) { return "kda-gb300 1.0 sm_103a"; }
 
-size_t kda_chunk_fwd_workspace_size(int, int, int, int, int) { return 0; }
-size_t kda_varlen_fwd_workspace_size(int, int, int, int, int) { return 0; }
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
+  (void)d_k;
+  (void)d_v;
+  if (B <= 0 || T <= 0 || H <= 0) return 0;
+  return kda::chunk_workspace_bytes(false, B, T, H);
+}
+size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v) {
+  (void)d_k;
+  (void)d_v;
+  if (N <= 0 || T_total <= 0 || H <= 0) return 0;
+  return kda::chunk_workspace_bytes(true, N, T_total, H);
+}
 
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const void* log_alpha,
                            const void* beta, const float* initial_state, void* out,
                            kda_dtype_t out_dtype, float* final_state, int B, int T, int H,
                            int d_k, int d_v, float scale, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
   kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
                                      final_state, H, d_k, d_v, (long long)B * T > 0);
   if (st != KDA_OK) return st;
   if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
   if (B == 0) return KDA_OK;
+  const size_t need = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v);
+  if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
                       final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env()};
-  return from_cuda(kda::launch_chunk_fwd(p, stream));
+  return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
 kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const void* log_alpha,
@@ -85,8 +96,6 @@ kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const v
                             kda_dtype_t out_dtype, float* final_state, int H, int d_k, int d_v,
                             float scale, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (!cu_seqlens || N < 0 || T_total < 0 || max_seqlen < 0) return KDA_ERR_INVALID_ARG;
   if (N > 0 && max_seqlen == 0 && T_total > 0) return KDA_ERR_INVALID_ARG;
   if (!aligned16(cu_seqlens)) return KDA_ERR_ALIGNMENT;
@@ -94,10 +103,13 @@ kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const v
                                      final_state, H, d_k, d_v, T_total > 0);
   if (st != KDA_OK) return st;
   if (N == 0) return KDA_OK;
+  const size_t need = kda_varlen_fwd_workspace_size(N, T_total, H, d_k, d_v);
+  if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
                       final_state, cu_seqlens, N, max_seqlen, T_total, H, d_k, scale,
                       check_decay_env()};
-  return from_cuda(kda::launch_chunk_fwd(p, stream));
+  return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* log_alpha,

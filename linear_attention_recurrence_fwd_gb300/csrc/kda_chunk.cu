@@ -1,9 +1,8 @@
-// Chunked KDA prefill on tcgen05 tensor cores.
+// Chunked KDA prefill on tcgen05 tensor cores, in two stages.
 //
-// One CTA (128 threads) walks one (sequence, head) through 64-token chunks
-// made of four 16-token tiles.  Per chunk, with g the cumulative log-decay
-// from the chunk start (per key channel, inclusive) and S the fp32 state
-// entering the chunk:
+// For a 64-token chunk (four 16-token tiles) of one (sequence, head), with
+// g the cumulative log-decay from the chunk start (per key channel,
+// inclusive) and S the fp32 state entering the chunk:
 //
 //   A_qk[r,i] = sum_c q_rc k_ic e^{g_rc - g_ic}          (i <= r)
 //   A_kk[r,i] = beta_r sum_c k_rc k_ic e^{g_rc - g_ic}   (i <  r)
@@ -19,28 +18,37 @@
 // column tile b with end reference E_b = g at its last token,
 //   e^{g_r - g_i} = e^{g_r - E_b} * e^{E_b - g_i},   i in tile b, r >= i,
 // has a left factor in [0, e^80] and a right factor in [e^-80, 1]: both fit
-// bf16/fp32.  So the DIAGONAL tiles use the same dense bf16 tcgen05 product
-// as the off-diagonal ones; there is no per-position-pair special path.
+// bf16/fp32.  So the DIAGONAL tiles use the same dense tcgen05 product as
+// the off-diagonal ones; there is no per-position-pair special path.
 //
-// Every product is a tcgen05.mma with M = 128 (fp32 accumulators in TMEM):
-//   M1 (x4) [Q^(b); K^(b)] (128 x d) . Kb[tile b]^T      -> A_qk | A_kk column tile b
-//   M2      (k e^g)^T (d x 64) . (T diag beta)^T        -> W^T
-//   M3      V^T . (T diag beta)^T                       -> U~^T
-//   M4      U^T  = U~^T - S^T W^T                       (negated A operand)
-//   M5      O^T  = S^T (q e^g)^T + U^T A_qk^T
-//   M6      S^T <- S^T Diag(e^{g_C}) + U^T K-bar
-// The state is kept transposed (S^T, value channel = TMEM lane) in TMEM as
-// an fp32 accumulator; its 16-bit copy in shared memory is the MMA operand.
+// Stage 1 (kda_intra_kernel) needs no state, so it runs one CTA per
+// (chunk, head) over every SM (two CTAs per SM).  It writes a per-chunk
+// record -- W, q e^g, k e^{g_C - g}, A_qk, T diag(beta) and e^{g_C} -- as
+// byte images of the shared-memory operand tiles stage 2 feeds its MMAs.
+// Stage 2 (kda_state_kernel) walks each (sequence, head) serially,
+// double-buffering records with bulk copies and v tiles with TMA:
+//   M3  U~^T = V^T (T diag beta)^T             bf16
+//   M4  U^T  = U~^T - S^T W^T                  fp16 (negated A)
+//   M5  O^T  = S^T (q e^g)^T + U^T A_qk^T      fp16
+//   M6  S^T <- S^T Diag(e^{g_C}) + U^T K-bar   fp16
+// with S^T (value channel = TMEM lane) as an fp32 TMEM accumulator and its
+// fp16 copy in shared memory as the MMA operand.
+//
+// Stage 1 products, all tcgen05 with M = 128:
+//   the cumulative sum g^T = LA^T L^T (L lower-triangular ones) and the
+//   transposes q^T = Q^T I, k^T = K^T I move per-channel columns into TMEM
+//   (one thread per key channel reads them back);
+//   M1 (x4) [Q^(b); K^(b)] . Kb[tile b]^T -> column tile b of [A_qk; A_kk];
+//   M2 (k e^g)^T (T diag beta)^T -> W^T.
+// The 64x64 unit lower-triangular inverse is formed in fp32 on CUDA cores.
 //
 // Precision.  The tile-referenced M1 operands span e^{+-80} and need bf16's
 // range; their 8-bit mantissa alone costs too much accuracy in A, so each is
 // split into a bf16 pair x = hi + lo and M1 accumulates hi.hi + lo.hi + hi.lo
-// (three MMAs per tile, fp32 accumulation).  Every state-pass operand (S, W,
-// q e^g, U, A_qk, k e^{g_C - g}) is bounded by O(1)..O(10) and is stored as
-// fp16 (3 more mantissa bits than bf16, same tensor-core rate).  The M2/M3
-// operands pair with the raw bf16 v tile and stay bf16.
-// The 64x64 unit lower-triangular inverse is formed in fp32 on CUDA cores
-// (16x16 diagonal blocks by forward substitution, then block products).
+// (fp32 accumulation).  Every state-pass operand (S, W, q e^g, U, A_qk,
+// k e^{g_C - g}) is bounded by O(1)..O(10) and is stored as fp16 (3 more
+// mantissa bits than bf16, same tensor-core rate).  T diag(beta) and
+// (k e^g)^T pair with the raw bf16 v tile / each other and stay bf16.
 //
 // d = 64 heads run the d = 128 code with the upper channel half zeroed.
 #include <cuda_bf16.h>
@@ -58,44 +66,40 @@ namespace {
 
 constexpr int CH = 64;   // tokens per chunk
 constexpr int DP = 128;  // padded head dimension
-constexpr int NTHREADS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Shared-memory map (bytes from a 1024-aligned base).
-constexpr uint32_t OFF_RQ = 0;        // raw q tile  [64 tok][128 ch], TMA, 128B swizzle
-constexpr uint32_t OFF_RK = 16384;    // raw k tile
-constexpr uint32_t OFF_RG = 32768;    // raw log_alpha tile
-constexpr uint32_t OFF_RV = 49152;    // raw v tile (also the V^T operand of M3)
-constexpr uint32_t OFF_XH = 65536;    // M1 A operand of the current tile version, hi part
-constexpr uint32_t OFF_XL = 98304;    // ... lo part
-constexpr uint32_t OFF_KT = 65536;    // (k e^g)^T          (after M1)
-constexpr uint32_t OFF_QT = 81920;    // (q e^g)            (after M1)
-constexpr uint32_t OFF_KBAR = 98304;  // k e^{g_C - g}       (after M1)
-constexpr uint32_t OFF_AKK = 114688;  // A_kk fp32 [64][64]  (after M1)
-constexpr uint32_t OFF_KB = 131072;   // M1 B operand: k e^{E_b - g}, hi part
-constexpr uint32_t OFF_KBL = 188416;  // ... lo part (shares the U^T buffer, free during M1)
-constexpr uint32_t OFF_WT = 131072;   // W (fp16)            (after M1)
-constexpr uint32_t OFF_TB = 147456;   // T diag(beta) (bf16)
-constexpr uint32_t OFF_ST = 155648;   // S^T (fp16), 2 K-blocks
-constexpr uint32_t OFF_UT = 188416;   // U^T (fp16)
-constexpr uint32_t OFF_AQ = 204800;   // A_qk (fp16)
-constexpr uint32_t OFF_TI = 212992;   // T fp32 [64][64]
-constexpr uint32_t SMEM_BYTES = 229376 + 1024;
+// ---- per-(chunk, head) record: stage 2's shared-memory operand images
+constexpr uint32_t REC_WT = 0;         // W (fp16), B operand: N = r, K = c, MN-major
+constexpr uint32_t REC_QT = 16384;     // q e^g (fp16), B operand: N = r, K = c, MN-major
+constexpr uint32_t REC_KBAR = 32768;   // k e^{g_C - g} (fp16), B operand: N = c, K = i
+constexpr uint32_t REC_AQ = 49152;     // A_qk (fp16), B operand: N = r, K = i
+constexpr uint32_t REC_TB = 57344;     // T diag(beta) (bf16), B operand: N = r, K = i
+constexpr uint32_t REC_G = 65536;      // e^{g_C} per key channel, fp32 x 128
+constexpr uint32_t REC_LOAD = 66048;   // bytes copied per record
+constexpr uint32_t REC_BYTES = 66560;  // record stride
 
-// TMEM columns.
-constexpr uint32_t TM_A = 0, TM_W = 64, TM_U = 128, TM_O = 192, TM_S = 256, TM_COLS = 512;
+// ---- stage 1 shared memory (bytes from a 1024-aligned base); phases reuse space
+constexpr uint32_t A_RQ = 0, A_RK = 16384, A_RG = 32768;  // raw TMA tiles   (transposes)
+constexpr uint32_t A_LM = 65536, A_IM = 73728;            // L, I (bf16)      (transposes)
+constexpr uint32_t A_XH = 0, A_XL = 32768;                // M1 A operand     (M1)
+constexpr uint32_t A_KBH = 65536, A_KBL = 81920;          // M1 B operand     (M1)
+constexpr uint32_t A_STG = 0;                             // record image [0, 64K) (after M1)
+constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][64]  (after M1)
+constexpr uint32_t A_KT = 81920;                          // (k e^g)^T bf16      (after M1)
+constexpr uint32_t A_TI = 0;                              // T fp32 (in the W slot, before W)
+constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
+constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
 
-struct Params {
-  const __nv_bfloat16* beta;
-  const float* s0;
-  void* out;
-  float* s1;
-  const int* cu;  // device cu_seqlens (packed) or null (fixed length)
-  int T;          // tokens per sequence when cu is null
-  int H;
-  float scale;
-  int check_decay;
-};
+// ---- stage 2 shared memory
+constexpr uint32_t B_REC0 = 0, B_V0 = 66560, B_REC1 = 82944, B_V1 = 149504;
+constexpr uint32_t B_ST = 165888;  // S^T fp16, 2 K-blocks
+constexpr uint32_t B_UT = 198656;  // U^T fp16
+constexpr uint32_t B_MISC = 215040;
+constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
+
+// ---- TMEM columns
+constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
+constexpr uint32_t TB_U = 0, TB_O = 64, TB_S = 128, TB_COLS = 256;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -140,12 +144,15 @@ __device__ __forceinline__ void st8h(uint32_t addr, const float* x) {
                pack_f16x2(x[6], x[7]));
 }
 // x as an unevaluated bf16 pair: hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void split_bf16(const float* x, float* hi, float* lo) {
+__device__ __forceinline__ void st8_split(uint32_t addr_hi, uint32_t addr_lo, const float* x) {
+  float hi[8], lo[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     hi[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
     lo[j] = x[j] - hi[j];
   }
+  st8(addr_hi, hi);
+  st8(addr_lo, lo);
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -164,138 +171,163 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   }
 }
 
+__device__ __forceinline__ void set_status(int code) { atomicExch(&g_chunk_status, code); }
+
+// Chunk -> (sequence, first token, valid tokens).  Packed sequences use the
+// per-sequence chunk offsets (chunk_base[n] = chunks before sequence n).
+struct ChunkLoc {
+  int n, j, t0, valid, ok;
+};
+__device__ __forceinline__ ChunkLoc locate_chunk(int q, const int* cu, const int* base, int n_seq,
+                                                 int T) {
+  ChunkLoc L;
+  int len, seq0;
+  if (cu) {
+    if (q >= base[n_seq]) {
+      L.ok = 0;
+      return L;
+    }
+    int lo = 0, hi = n_seq;  // base[lo] <= q < base[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (base[mid] <= q) lo = mid; else hi = mid;
+    }
+    L.n = lo;
+    L.j = q - base[lo];
+    seq0 = cu[lo];
+    len = cu[lo + 1] - seq0;
+  } else {
+    const int nc = (T + CH - 1) / CH;
+    L.n = q / nc;
+    L.j = q % nc;
+    seq0 = L.n * T;
+    len = T;
+  }
+  L.t0 = seq0 + CH * L.j;
+  L.valid = min(CH, len - CH * L.j);
+  L.ok = 1;
+  return L;
+}
+
 // Version b of the M1 A operand: rows r >= 16 b of [Q^(b); K^(b)] with
-// Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r F[tile(r)][b] (same for K).
-// Rows above 16 b are never read back (their products are masked).
+// Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r F[tile(r)][b] (same for K),
+// as bf16 hi/lo pairs.  Rows above 16 b are never read back.
 template <int B>
-__device__ __forceinline__ void build_version(const OperandLayout& LXh, const OperandLayout& LXl,
-                                              const OperandLayout& LQ, const OperandLayout& LK,
-                                              int c, int valid, const float (&p)[CH],
+__device__ __forceinline__ void build_version(const OperandLayout& XH, const OperandLayout& XL,
+                                              uint32_t tl, int c, const float (&p)[CH],
                                               const float (&F)[4][4]) {
 #pragma unroll
-  for (int r0 = 16 * B; r0 < CH; r0 += 8) {
-    float fq[8], fk[8], hi[8], lo[8];
+  for (int a = B; a < 4; ++a) {
+    float qv[16], kv[16];
+    tmem_ld16(tl + TA_Q + 16 * a, qv);
+    tmem_ld16(tl + TA_K + 16 * a, kv);
+    tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r = r0 + j;
-      const float f = p[r] * F[r / 16][B];
-      const bool ok = r < valid;
-      fq[j] = ok ? bf2f(ld_shared_u16(layout_addr(LQ, r, c))) * f : 0.f;
-      fk[j] = ok ? bf2f(ld_shared_u16(layout_addr(LK, r, c))) * f : 0.f;
+    for (int h8 = 0; h8 < 16; h8 += 8) {
+      float fq[8], fk[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float f = p[16 * a + h8 + j] * F[a][B];
+        fq[j] = qv[h8 + j] * f;
+        fk[j] = kv[h8 + j] * f;
+      }
+      const int r0 = 16 * a + h8;
+      st8_split(layout_addr(XH, r0, c), layout_addr(XL, r0, c), fq);
+      st8_split(layout_addr(XH, CH + r0, c), layout_addr(XL, CH + r0, c), fk);
     }
-    split_bf16(fq, hi, lo);
-    st8(layout_addr(LXh, r0, c), hi);
-    st8(layout_addr(LXl, r0, c), lo);
-    split_bf16(fk, hi, lo);
-    st8(layout_addr(LXh, CH + r0, c), hi);
-    st8(layout_addr(LXl, CH + r0, c), lo);
   }
 }
 
-template <int DIN, typename OutT>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    kda_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                     Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ uint64_t tma_bar, mma_bar;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ float s_beta[CH];
-  __shared__ float s_gamma[DP];
-  __shared__ int s_abort;
+struct IntraParams {
+  const __nv_bfloat16* beta;
+  uint8_t* records;
+  const int* cu;
+  const int* chunk_base;
+  int T, n_seq, H;
+  int check_decay;
+};
 
+template <int DIN>
+__global__ void __launch_bounds__(128, 2)
+    kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
+  const ChunkLoc loc = locate_chunk(blockIdx.x, p.cu, p.chunk_base, p.n_seq, p.T);
+  if (!loc.ok) return;  // packed grids are sized for the worst case
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.x, n = blockIdx.y;
-  const int H = p.H;
+  const int h = blockIdx.y, H = p.H, valid = loc.valid;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sbp = smem_raw + (sb - raw);
-
-  int tok0, len;
-  if (p.cu) {
-    tok0 = p.cu[n];
-    len = p.cu[n + 1] - tok0;
-  } else {
-    tok0 = n * p.T;
-    len = p.T;
-  }
-  const int nchunks = len > 0 ? (len + CH - 1) / CH : 0;
-
-  const OperandLayout L_RQ = kmajor(sb + OFF_RQ, 8192), L_RK = kmajor(sb + OFF_RK, 8192);
-  const OperandLayout L_RG = kmajor(sb + OFF_RG, 8192);
-  const OperandLayout L_VA = mnmajor(sb + OFF_RV, 8192);   // M = v, K = i
-  const OperandLayout L_XH = mnmajor(sb + OFF_XH, 16384);  // M = [q r; k r], K = c
-  const OperandLayout L_XL = mnmajor(sb + OFF_XL, 16384);
-  const OperandLayout L_KB = mnmajor(sb + OFF_KB, 16384);   // N = i, K = c
-  const OperandLayout L_KBL = mnmajor(sb + OFF_KBL, 16384);
-  const OperandLayout L_TB = kmajor(sb + OFF_TB, 0);       // N = r, K = i
-  const OperandLayout L_KT = kmajor(sb + OFF_KT, 0);       // M = c, K = i
-  const OperandLayout L_QT = mnmajor(sb + OFF_QT, 16384);  // N = r, K = c
-  const OperandLayout L_WT = mnmajor(sb + OFF_WT, 16384);  // N = r, K = c
-  const OperandLayout L_KBAR = kmajor(sb + OFF_KBAR, 0);   // N = c, K = i
-  const OperandLayout L_ST = kmajor(sb + OFF_ST, 16384);   // M = v, K = c
-  const OperandLayout L_UT = kmajor(sb + OFF_UT, 0);       // M = v, K = i
-  const OperandLayout L_AQ = kmajor(sb + OFF_AQ, 0);       // N = r, K = i
-  float* akk = reinterpret_cast<float*>(sbp + OFF_AKK);
-  float* ti = reinterpret_cast<float*>(sbp + OFF_TI);
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sbp + A_MISC);
+  uint64_t* bar_mma = bar_tma + 1;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + A_MISC + 16);
+  int* s_abort = reinterpret_cast<int*>(sbp + A_MISC + 20);
+  float* s_beta = reinterpret_cast<float*>(sbp + A_MISC + 64);    // [64]
+  float* s_gamma = reinterpret_cast<float*>(sbp + A_MISC + 512);  // [128], 16-byte aligned
+  uint8_t* rec = p.records + ((size_t)blockIdx.x * H + h) * REC_BYTES;
 
   if (tid == 0) {
-    mbar_init(&tma_bar, 1);
-    mbar_init(&mma_bar, 1);
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
     mbar_fence_init();
-    s_abort = 0;
+    *s_abort = 0;
+    mbar_arrive_expect_tx(bar_tma, 3u * (DIN / 64) * 8192u);
+#pragma unroll
+    for (int b = 0; b < DIN / 64; ++b) {
+      tma_load_3d(sbp + A_RQ + b * 8192, &tm_q, bar_tma, b * 64, h, loc.t0);
+      tma_load_3d(sbp + A_RK + b * 8192, &tm_k, bar_tma, b * 64, h, loc.t0);
+      tma_load_3d(sbp + A_RG + b * 8192, &tm_g, bar_tma, b * 64, h, loc.t0);
+    }
   }
-  if (DIN == 64) {  // the upper channel half of every raw tile stays zero
-    for (uint32_t off = tid * 16; off < 8192; off += NTHREADS * 16) {
-      st_shared_v4(sb + OFF_RQ + 8192 + off, 0, 0, 0, 0);
-      st_shared_v4(sb + OFF_RK + 8192 + off, 0, 0, 0, 0);
-      st_shared_v4(sb + OFF_RG + 8192 + off, 0, 0, 0, 0);
-      st_shared_v4(sb + OFF_RV + 8192 + off, 0, 0, 0, 0);
+  if (DIN == 64) {  // upper channel half of the raw tiles stays zero
+    for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
+      st_shared_v4(sb + A_RQ + 8192 + off, 0, 0, 0, 0);
+      st_shared_v4(sb + A_RK + 8192 + off, 0, 0, 0, 0);
+      st_shared_v4(sb + A_RG + 8192 + off, 0, 0, 0, 0);
+    }
+  }
+  if (tid < CH)
+    s_beta[tid] = tid < valid ? __bfloat162float(p.beta[(size_t)(loc.t0 + tid) * H + h]) : 0.f;
+  // L[r][i] = (i <= r), I[r][i] = (i == r), both restricted to valid tokens i
+  const OperandLayout LM = kmajor(sb + A_LM, 0), IM = kmajor(sb + A_IM, 0);
+  {
+    const int r = tid >> 1, i_lo = (tid & 1) * 32;
+#pragma unroll
+    for (int i0 = i_lo; i0 < i_lo + 32; i0 += 8) {
+      float l[8], e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j;
+        l[j] = (i <= r && i < valid) ? 1.f : 0.f;
+        e[j] = (i == r && i < valid) ? 1.f : 0.f;
+      }
+      st8(layout_addr(LM, r, i0), l);
+      st8(layout_addr(IM, r, i0), e);
     }
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base_s, TM_COLS);
+    tmem_alloc(tmem_base_s, TA_COLS);
     tmem_relinquish();
   }
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = tmem_base_s;
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 TMEM lanes
+  const uint32_t tmem = *tmem_base_s;
+  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+  uint32_t mma_phase = 0;
 
-  uint32_t tma_phase = 0, mma_phase = 0;
-  bool tma_pending = false;
-  constexpr uint32_t kTxBytes = 4u * (DIN / 64) * 8192u;
-  auto issue_loads = [&](int chunk) {
-    const int t = tok0 + chunk * CH;
-    mbar_arrive_expect_tx(&tma_bar, kTxBytes);
-#pragma unroll
-    for (int b = 0; b < DIN / 64; ++b) {
-      tma_load_3d(sbp + OFF_RQ + b * 8192, &tm_q, &tma_bar, b * 64, h, t);
-      tma_load_3d(sbp + OFF_RK + b * 8192, &tm_k, &tma_bar, b * 64, h, t);
-      tma_load_3d(sbp + OFF_RG + b * 8192, &tm_g, &tma_bar, b * 64, h, t);
-      tma_load_3d(sbp + OFF_RV + b * 8192, &tm_v, &tma_bar, b * 64, h, t);
-    }
-  };
-  if (nchunks > 0) {
-    if (tid == 0) issue_loads(0);
-    tma_pending = true;
-  }
-
-  // Bounded wait on a barrier by every thread; a timeout anywhere aborts the CTA.
   auto wait_all = [&](uint64_t* bar, uint32_t& phase) -> bool {
-    const bool ok = mbar_wait(bar, phase);
-    if (!ok) {
-      s_abort = 1;
-      atomicExch(&g_chunk_status, 6);
+    if (!mbar_wait(bar, phase)) {
+      *s_abort = 1;
+      set_status(6);
     }
     phase ^= 1u;
     __syncthreads();
     tc_fence_after_sync();
-    return s_abort == 0;
+    return *s_abort == 0;
   };
-  // Make this thread's smem operand writes visible to the tensor core and
-  // meet the other threads before thread 0 issues MMAs.
   auto operands_ready = [&]() {
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -303,114 +335,104 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after_sync();
   };
 
-  // Initial state: thread v holds row v of S^T.
-  {
-    const int v = tid;
-    const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
-#pragma unroll
-    for (int c0 = 0; c0 < DP; c0 += 16) {
-      float s[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = c0 + j;
-        s[j] = (p.s0 && c < DIN && v < DIN) ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
-      }
-      tmem_st16(tl + TM_S + c0, s);
-      st8h(layout_addr(L_ST, v, c0), s);
-      st8h(layout_addr(L_ST, v, c0 + 8), s + 8);
-    }
-    tmem_st_wait();
-  }
-
-  constexpr uint32_t ID_M1 = make_idesc(128, 16, true, true);                // bf16
-  constexpr uint32_t ID_W = make_idesc(128, 64, false, false);               // bf16
-  constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                // bf16
-  constexpr uint32_t ID_U = make_idesc(128, 64, false, true, true, true);    // fp16, -A
-  constexpr uint32_t ID_O1 = make_idesc(128, 64, false, true, false, true);  // fp16
-  constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, false, true); // fp16
-  constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true); // fp16
-
+  uint32_t tma_phase = 0;
+  bool ok = wait_all(bar_tma, tma_phase);
   const int c = tid;  // key channel owned in the elementwise stages
-  for (int chunk = 0; chunk < nchunks; ++chunk) {
-    const int t0 = tok0 + chunk * CH;
-    const int valid = min(CH, len - chunk * CH);
-
-    if (tid < CH) s_beta[tid] = tid < valid ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-    if (!wait_all(&tma_bar, tma_phase)) break;
-    tma_pending = false;
-
-    // ---- cumulative log-decay and per-tile references (thread = channel c)
-    float pr[CH];  // p_r = e^{g_r - E_tile(r)} in [1, e^80]
-    float E[4];
-    {
-      float acc = 0.f;
-      bool bad = false;
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        float la = bf2f(ld_shared_u16(layout_addr(L_RG, i, c)));
-        la = i < valid ? la : 0.f;
-        bad |= !(la >= -5.f && la <= 0.f);
-        acc += la;
-        pr[i] = acc;
-      }
-      if (p.check_decay && bad) atomicExch(&g_chunk_status, 5);
-#pragma unroll
-      for (int b = 0; b < 4; ++b) E[b] = pr[16 * b + 15];
-#pragma unroll
-      for (int i = 0; i < CH; ++i) pr[i] = ex2((pr[i] - E[i / 16]) * LOG2E);
+  if (ok && p.check_decay) {
+    bool bad = false;
+    const OperandLayout RG = kmajor(sb + A_RG, 8192);
+    for (int i = 0; i < valid; ++i) {
+      const float la = bf2f(ld_shared_u16(layout_addr(RG, i, c)));
+      bad |= !(la >= -5.f && la <= 0.f);
     }
-    float F[4][4];  // F[a][b] = e^{E_a - E_b} (a >= b)
+    if (bad) set_status(5);
+  }
+  constexpr uint32_t ID_T = make_idesc(128, 64, true, false);  // bf16, A MN-major
+  if (ok && tid == 0) {
+    const OperandLayout RQ = mnmajor(sb + A_RQ, 8192), RK = mnmajor(sb + A_RK, 8192);
+    const OperandLayout RG = mnmajor(sb + A_RG, 8192);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int k0 = 0; k0 < CH; k0 += 16) {
+      umma_bf16(tmem + TA_G, layout_desc(RG, 0, k0), layout_desc(LM, 0, k0), ID_T, k0 > 0);
+      umma_bf16(tmem + TA_Q, layout_desc(RQ, 0, k0), layout_desc(IM, 0, k0), ID_T, k0 > 0);
+      umma_bf16(tmem + TA_K, layout_desc(RK, 0, k0), layout_desc(IM, 0, k0), ID_T, k0 > 0);
+    }
+    umma_commit(bar_mma);
+  }
+  if (ok) ok = wait_all(bar_mma, mma_phase);
+
+  // ---- per-channel decay factors (thread = channel c, TMEM lane c)
+  float pr[CH], F[4][4], GE[4];
+  if (ok) {
+    float g[CH];
+    tmem_ld64(tl + TA_G, g);
+    float E[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) E[b] = g[16 * b + 15];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) pr[i] = ex2((g[i] - E[i / 16]) * LOG2E);  // [1, e^80]
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      GE[a] = ex2(E[a] * LOG2E);
 #pragma unroll
       for (int b = 0; b < 4; ++b) F[a][b] = a > b ? ex2((E[a] - E[b]) * LOG2E) : 1.f;
-    float GE[4];  // e^{E_a}
-#pragma unroll
-    for (int a = 0; a < 4; ++a) GE[a] = ex2(E[a] * LOG2E);
-
-    // ---- M1: column tile b of [A_qk; A_kk] = [Q^(b); K^(b)] . Kb[tile b]^T, with
-    // each factor as a bf16 pair (hi.hi + lo.hi + hi.lo), one tile version at a time
-#pragma unroll
-    for (int i0 = 0; i0 < CH; i0 += 8) {
-      float fk[8], hi[8], lo[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j;
-        fk[j] = i < valid ? bf2f(ld_shared_u16(layout_addr(L_RK, i, c))) * rcp(pr[i]) : 0.f;
-      }
-      split_bf16(fk, hi, lo);
-      st8(layout_addr(L_KB, i0, c), hi);
-      st8(layout_addr(L_KBL, i0, c), lo);
     }
-    bool m1_ok = true;
+  }
+
+  // ---- M1: column tile b of [A_qk; A_kk], one tile version at a time
+  const OperandLayout XH = mnmajor(sb + A_XH, 16384), XL = mnmajor(sb + A_XL, 16384);
+  const OperandLayout KBH = mnmajor(sb + A_KBH, 16384), KBL = mnmajor(sb + A_KBL, 16384);
+  constexpr uint32_t ID_M1 = make_idesc(128, 16, true, true);
+  if (ok) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      if (b == 0) build_version<0>(L_XH, L_XL, L_RQ, L_RK, c, valid, pr, F);
-      if (b == 1) build_version<1>(L_XH, L_XL, L_RQ, L_RK, c, valid, pr, F);
-      if (b == 2) build_version<2>(L_XH, L_XL, L_RQ, L_RK, c, valid, pr, F);
-      if (b == 3) build_version<3>(L_XH, L_XL, L_RQ, L_RK, c, valid, pr, F);
-      operands_ready();
-      if (tid == 0) {
-        const uint32_t d = tmem + TM_A + 16 * b;
+    for (int a = 0; a < 4; ++a) {
+      float kv[16];
+      tmem_ld16(tl + TA_K + 16 * a, kv);
+      tmem_ld_wait();
 #pragma unroll
-        for (int k0 = 0; k0 < DP; k0 += 16) {
-          umma_bf16(d, layout_desc(L_XH, 0, k0), layout_desc(L_KB, 16 * b, k0), ID_M1, k0 > 0);
-          umma_bf16(d, layout_desc(L_XL, 0, k0), layout_desc(L_KB, 16 * b, k0), ID_M1, 1);
-          umma_bf16(d, layout_desc(L_XH, 0, k0), layout_desc(L_KBL, 16 * b, k0), ID_M1, 1);
-        }
-        umma_commit(&mma_bar);
-      }
-      if (!wait_all(&mma_bar, mma_phase)) {
-        m1_ok = false;
-        break;
+      for (int h8 = 0; h8 < 16; h8 += 8) {
+        float fk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) fk[j] = kv[h8 + j] * rcp(pr[16 * a + h8 + j]);
+        const int i0 = 16 * a + h8;
+        st8_split(layout_addr(KBH, i0, c), layout_addr(KBL, i0, c), fk);
       }
     }
-    if (!m1_ok) break;
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    if (!ok) break;
+    if (b == 0) build_version<0>(XH, XL, tl, c, pr, F);
+    if (b == 1) build_version<1>(XH, XL, tl, c, pr, F);
+    if (b == 2) build_version<2>(XH, XL, tl, c, pr, F);
+    if (b == 3) build_version<3>(XH, XL, tl, c, pr, F);
+    operands_ready();
+    if (tid == 0) {
+      const uint32_t d = tmem + TA_A + 16 * b;
+#pragma unroll
+      for (int k0 = 0; k0 < DP; k0 += 16) {
+        umma_bf16(d, layout_desc(XH, 0, k0), layout_desc(KBH, 16 * b, k0), ID_M1, k0 > 0);
+        umma_bf16(d, layout_desc(XL, 0, k0), layout_desc(KBH, 16 * b, k0), ID_M1, 1);
+        umma_bf16(d, layout_desc(XH, 0, k0), layout_desc(KBL, 16 * b, k0), ID_M1, 1);
+      }
+      umma_commit(bar_mma);
+    }
+    ok = wait_all(bar_mma, mma_phase);
+  }
 
-    // ---- A_qk (fp16 operand) and beta-scaled strictly-lower A_kk (fp32)
+  float* akk = reinterpret_cast<float*>(sbp + A_AKK);
+  float* ti = reinterpret_cast<float*>(sbp + A_TI);
+  const OperandLayout AQ = kmajor(sb + A_STG + REC_AQ, 0);
+  const OperandLayout QT = mnmajor(sb + A_STG + REC_QT, 16384);
+  const OperandLayout KBAR = kmajor(sb + A_STG + REC_KBAR, 0);
+  const OperandLayout KT = kmajor(sb + A_KT, 0);
+  const OperandLayout TB = kmajor(sb + A_STG + REC_TB, 0);
+  const OperandLayout WT = mnmajor(sb + A_STG + REC_WT, 16384);
+  if (ok) {
+    // ---- A_qk (fp16 record image) and beta-scaled strictly-lower A_kk (fp32)
     {
       float a[64];
-      tmem_ld64(tl + TM_A, a);
+      tmem_ld64(tl + TA_A, a);
       if (warp < 2) {
         const int r = tid;
 #pragma unroll
@@ -418,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           float x[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) x[j] = (i0 + j <= r) ? a[i0 + j] : 0.f;
-          st8h(layout_addr(L_AQ, r, i0), x);
+          st8h(layout_addr(AQ, r, i0), x);
         }
       } else {
         const int r = tid - CH;
@@ -435,27 +457,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    // ---- state-pass operands (thread = channel c): (k e^g)^T, q e^g, k e^{g_C - g}
+    // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
 #pragma unroll
-    for (int i0 = 0; i0 < CH; i0 += 8) {
-      float kt[8], qt[8], kb[8];
+    for (int a = 0; a < 4; ++a) {
+      float qv[16], kv[16];
+      tmem_ld16(tl + TA_Q + 16 * a, qv);
+      tmem_ld16(tl + TA_K + 16 * a, kv);
+      tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j, a = i / 16;
-        const bool ok = i < valid;
-        const float kv = ok ? bf2f(ld_shared_u16(layout_addr(L_RK, i, c))) : 0.f;
-        const float qv = ok ? bf2f(ld_shared_u16(layout_addr(L_RQ, i, c))) : 0.f;
-        const float gam = pr[i] * GE[a];
-        kt[j] = kv * gam;
-        qt[j] = qv * gam;
-        kb[j] = kv * rcp(pr[i]) * F[3][a];
+      for (int h8 = 0; h8 < 16; h8 += 8) {
+        float kt[8], qt[8], kb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = 16 * a + h8 + j;
+          const float gam = pr[i] * GE[a];  // e^{g_i}
+          kt[j] = kv[h8 + j] * gam;
+          qt[j] = qv[h8 + j] * gam;
+          kb[j] = kv[h8 + j] * rcp(pr[i]) * F[3][a];  // e^{g_C - g_i}
+        }
+        const int i0 = 16 * a + h8;
+        st8(layout_addr(KT, c, i0), kt);
+        st8h(layout_addr(QT, i0, c), qt);
+        st8h(layout_addr(KBAR, c, i0), kb);
       }
-      st8(layout_addr(L_KT, c, i0), kt);     // bf16: pairs with T diag(beta)
-      st8h(layout_addr(L_QT, i0, c), qt);
-      st8h(layout_addr(L_KBAR, c, i0), kb);
     }
     s_gamma[c] = GE[3];
+    fence_proxy_async_smem();
     __syncthreads();
+    if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
+      bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
+      bulk_commit();
+    }
 
     // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by forward substitution
     if (tid < 64) {
@@ -477,7 +509,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll 1
     for (int s = 1; s < 4; ++s) {
       const int nel = (4 - s) * 256;
-      for (int e = tid; e < nel; e += NTHREADS) {
+      for (int e = tid; e < nel; e += 128) {
         const int b = e >> 8, a = b + s, rr = (e >> 4) & 15, cc = e & 15;
         float acc = 0.f;
         for (int m = b; m < a; ++m)
@@ -487,7 +519,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ti[(16 * b + rr) * CH + 16 * a + cc] = acc;  // scratch in the (zero) upper triangle
       }
       __syncthreads();
-      for (int e = tid; e < nel; e += NTHREADS) {
+      for (int e = tid; e < nel; e += 128) {
         const int b = e >> 8, a = b + s, rr = (e >> 4) & 15, cc = e & 15;
         float acc = 0.f;
         for (int x = 0; x <= rr; ++x)
@@ -507,82 +539,226 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int i = i0 + j;
           x[j] = i <= r ? ti[r * CH + i] * s_beta[i] : 0.f;
         }
-        st8(layout_addr(L_TB, r, i0), x);
+        st8(layout_addr(TB, r, i0), x);
       }
     }
     operands_ready();
     if (tid == 0) {
+      constexpr uint32_t ID_W = make_idesc(128, 64, false, false);
 #pragma unroll
-      for (int k0 = 0; k0 < CH; k0 += 16) {
-        umma_bf16(tmem + TM_W, layout_desc(L_KT, 0, k0), layout_desc(L_TB, 0, k0), ID_W, k0 > 0);
-        umma_bf16(tmem + TM_U, layout_desc(L_VA, 0, k0), layout_desc(L_TB, 0, k0), ID_V, k0 > 0);
-      }
-      umma_commit(&mma_bar);
+      for (int k0 = 0; k0 < CH; k0 += 16)
+        umma_bf16(tmem + TA_W, layout_desc(KT, 0, k0), layout_desc(TB, 0, k0), ID_W, k0 > 0);
+      umma_commit(bar_mma);
     }
-    if (!wait_all(&mma_bar, mma_phase)) break;
-    // raw tiles are consumed: fetch the next chunk while the state pass runs
-    if (chunk + 1 < nchunks) {
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        issue_loads(chunk + 1);
-      }
-      tma_pending = true;
+    ok = wait_all(bar_mma, mma_phase);
+  }
+  if (ok) {
+    // ---- W (fp16, N = r, K = c) from W^T in TMEM (lane = c), into the T slot
+    float w[64];
+    tmem_ld64(tl + TA_W, w);
+#pragma unroll
+    for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(WT, r0, c), w + r0);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(rec + REC_WT, sb + A_STG + REC_WT, REC_QT - REC_WT);
+      bulk_s2g(rec + REC_TB, sb + A_STG + REC_TB, REC_G - REC_TB);
+      bulk_s2g(rec + REC_G, smem_u32(s_gamma), 512);
+      bulk_commit();
     }
+  }
+  if (tid == 0) bulk_wait_all();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TA_COLS);
+}
 
-    // ---- W (fp16, N = r, K = c) from W^T in TMEM (lane = c)
-    {
-      float w[64];
-      tmem_ld64(tl + TM_W, w);
+struct StateParams {
+  const uint8_t* records;
+  const float* s0;
+  float* s1;
+  void* out;
+  const int* cu;
+  const int* chunk_base;
+  int T, n_seq, H;
+  float scale;
+};
+
+template <int DIN, typename OutT>
+__global__ void __launch_bounds__(128, 1)
+    kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.x, n = blockIdx.y, H = p.H;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sbp = smem_raw + (sb - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbp + B_MISC);  // [2]
+  uint64_t* bar_mma = full + 2;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 32);
+  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 36);
+
+  int tok0, len, base;
+  if (p.cu) {
+    tok0 = p.cu[n];
+    len = p.cu[n + 1] - tok0;
+    base = p.chunk_base[n];
+  } else {
+    tok0 = n * p.T;
+    len = p.T;
+    base = n * ((p.T + CH - 1) / CH);
+  }
+  const int nchunks = len > 0 ? (len + CH - 1) / CH : 0;
+  constexpr uint32_t kVBytes = (DIN / 64) * 8192u;
+
+  auto issue_loads = [&](int j, int buf) {
+    const uint8_t* rec = p.records + ((size_t)(base + j) * H + h) * REC_BYTES;
+    uint8_t* dst = sbp + (buf ? B_REC1 : B_REC0);
+    uint8_t* vdst = sbp + (buf ? B_V1 : B_V0);
+    mbar_arrive_expect_tx(&full[buf], REC_LOAD + kVBytes);
+    bulk_g2s(dst, rec, REC_LOAD, &full[buf]);
 #pragma unroll
-      for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(L_WT, r0, c), w + r0);
+    for (int b = 0; b < DIN / 64; ++b)
+      tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * j);
+  };
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(bar_mma, 1);
+    mbar_fence_init();
+    *s_abort = 0;
+    if (nchunks > 0) issue_loads(0, 0);
+    if (nchunks > 1) issue_loads(1, 1);
+  }
+  if (DIN == 64) {
+    for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
+      st_shared_v4(sb + B_V0 + 8192 + off, 0, 0, 0, 0);
+      st_shared_v4(sb + B_V1 + 8192 + off, 0, 0, 0, 0);
     }
-    operands_ready();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_base_s, TB_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_base_s;
+  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+  const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
+  const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
+
+  // initial state: thread v holds row v of S^T
+  const int v = tid;
+  const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+#pragma unroll
+  for (int c0 = 0; c0 < DP; c0 += 16) {
+    float s[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = c0 + j;
+      s[j] = (p.s0 && c < DIN && v < DIN) ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
+    }
+    tmem_st16(tl + TB_S + c0, s);
+    st8h(layout_addr(ST, v, c0), s);
+    st8h(layout_addr(ST, v, c0 + 8), s + 8);
+  }
+  tmem_st_wait();
+
+  auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
+    if (!mbar_wait(bar, phase)) {
+      *s_abort = 1;
+      set_status(6);
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    return *s_abort == 0;
+  };
+  auto operands_ready = [&]() {
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+  };
+  operands_ready();
+
+  constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
+  constexpr uint32_t ID_U = make_idesc(128, 64, false, true, true, true);     // fp16, -A
+  constexpr uint32_t ID_O1 = make_idesc(128, 64, false, true, false, true);   // fp16
+  constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, false, true);  // fp16
+  constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
+  uint32_t mma_phase = 0;
+  bool ok = true;
+  int pending = min(nchunks, 2);  // record loads in flight
+
+  for (int j = 0; j < nchunks && ok; ++j) {
+    const int buf = j & 1;
+    const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
+    const uint32_t vb = sb + (buf ? B_V1 : B_V0);
+    const float* gam = reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
+    const int valid = min(CH, len - CH * j);
+    if (!(ok = wait_all(&full[buf], (j >> 1) & 1))) break;
+    --pending;
+    const OperandLayout VA = mnmajor(vb, 8192);
+    const OperandLayout TB = kmajor(rb + REC_TB, 0), WT = mnmajor(rb + REC_WT, 16384);
+    const OperandLayout QT = mnmajor(rb + REC_QT, 16384), AQ = kmajor(rb + REC_AQ, 0);
+    const OperandLayout KBAR = kmajor(rb + REC_KBAR, 0);
     if (tid == 0) {
+#pragma unroll
+      for (int k0 = 0; k0 < CH; k0 += 16)
+        umma_bf16(tmem + TB_U, layout_desc(VA, 0, k0), layout_desc(TB, 0, k0), ID_V, k0 > 0);
 #pragma unroll
       for (int k0 = 0; k0 < DP; k0 += 16) {
-        umma_bf16(tmem + TM_U, layout_desc(L_ST, 0, k0), layout_desc(L_WT, 0, k0), ID_U, 1);
-        umma_bf16(tmem + TM_O, layout_desc(L_ST, 0, k0), layout_desc(L_QT, 0, k0), ID_O1, k0 > 0);
+        umma_bf16(tmem + TB_U, layout_desc(ST, 0, k0), layout_desc(WT, 0, k0), ID_U, 1);
+        umma_bf16(tmem + TB_O, layout_desc(ST, 0, k0), layout_desc(QT, 0, k0), ID_O1, k0 > 0);
       }
-      umma_commit(&mma_bar);
+      umma_commit(bar_mma);
     }
-    if (!wait_all(&mma_bar, mma_phase)) break;
-
-    // ---- U^T (fp16 operand) and the chunk decay of the fp32 state
+    // decay the fp32 state by e^{g_C} while the tensor core works on U and O
+#pragma unroll
+    for (int c0 = 0; c0 < DP; c0 += 16) {
+      float s[16];
+      tmem_ld16(tl + TB_S + c0, s);
+      tmem_ld_wait();
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) s[jj] *= gam[c0 + jj];
+      tmem_st16(tl + TB_S + c0, s);
+    }
+    tmem_st_wait();
+    if (!(ok = wait_all(bar_mma, mma_phase))) break;
+    mma_phase ^= 1u;
     {
-      const int v = tid;
       float u[64];
-      tmem_ld64(tl + TM_U, u);
+      tmem_ld64(tl + TB_U, u);
 #pragma unroll
-      for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(L_UT, v, r0), u + r0);
-#pragma unroll
-      for (int c0 = 0; c0 < DP; c0 += 16) {
-        float s[16];
-        tmem_ld16(tl + TM_S + c0, s);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) s[j] *= s_gamma[c0 + j];
-        tmem_st16(tl + TM_S + c0, s);
-      }
-      tmem_st_wait();
+      for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(UT, v, r0), u + r0);
     }
     operands_ready();
     if (tid == 0) {
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
-        umma_bf16(tmem + TM_O, layout_desc(L_UT, 0, k0), layout_desc(L_AQ, 0, k0), ID_O2, 1);
-        umma_bf16(tmem + TM_S, layout_desc(L_UT, 0, k0), layout_desc(L_KBAR, 0, k0), ID_S, 1);
+        umma_bf16(tmem + TB_O, layout_desc(UT, 0, k0), layout_desc(AQ, 0, k0), ID_O2, 1);
+        umma_bf16(tmem + TB_S, layout_desc(UT, 0, k0), layout_desc(KBAR, 0, k0), ID_S, 1);
       }
-      umma_commit(&mma_bar);
+      umma_commit(bar_mma);
     }
-    if (!wait_all(&mma_bar, mma_phase)) break;
-
-    // ---- outputs and the fp16 state operand for the next chunk (thread = value channel)
+    if (!(ok = wait_all(bar_mma, mma_phase))) break;
+    mma_phase ^= 1u;
+    if (j + 2 < nchunks) {  // this buffer is consumed: fetch chunk j + 2 into it
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        issue_loads(j + 2, buf);
+      }
+      ++pending;
+    }
+    // outputs, and the fp16 state operand for the next chunk
     {
-      const int v = tid;
       float o[64];
-      tmem_ld64(tl + TM_O, o);
+      tmem_ld64(tl + TB_O, o);
       if (v < DIN) {
-        OutT* out = static_cast<OutT*>(p.out) + (size_t)t0 * H * DIN + (size_t)h * DIN + v;
+        OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * j) * H * DIN +
+                    (size_t)h * DIN + v;
 #pragma unroll
         for (int r = 0; r < CH; ++r)
           if (r < valid) store_out(out + (size_t)r * H * DIN, p.scale * o[r]);
@@ -590,54 +766,123 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int c0 = 0; c0 < DP; c0 += 16) {
         float s[16];
-        tmem_ld16(tl + TM_S + c0, s);
+        tmem_ld16(tl + TB_S + c0, s);
         tmem_ld_wait();
-        st8h(layout_addr(L_ST, v, c0), s);
-        st8h(layout_addr(L_ST, v, c0 + 8), s + 8);
+        st8h(layout_addr(ST, v, c0), s);
+        st8h(layout_addr(ST, v, c0 + 8), s + 8);
       }
     }
+    operands_ready();
   }
 
-  if (s_abort == 0 && p.s1) {  // final state from the fp32 accumulator: S[c][v] = S^T[v][c]
-    const int v = tid;
-    const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+  if (ok && p.s1) {  // final state from the fp32 accumulator: S[c][v] = S^T[v][c]
 #pragma unroll
     for (int c0 = 0; c0 < DP; c0 += 16) {
       float s[16];
-      tmem_ld16(tl + TM_S + c0, s);
+      tmem_ld16(tl + TB_S + c0, s);
       tmem_ld_wait();
       if (v < DIN)
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < DIN) p.s1[sbase + (size_t)(c0 + j) * DIN + v] = s[j];
+        for (int jj = 0; jj < 16; ++jj)
+          if (c0 + jj < DIN) p.s1[sbase + (size_t)(c0 + jj) * DIN + v] = s[jj];
     }
   }
-  if (s_abort && tma_pending) mbar_wait(&tma_bar, tma_phase);  // let an issued copy land
+  if (!ok) {  // let copies already issued land before the CTA's memory goes away
+    for (int j = 0; j < 2 && pending > 0; ++j, --pending) mbar_wait(&full[j], 0, 100000000ull);
+  }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+  if (warp == 0) tmem_dealloc(tmem, TB_COLS);
+}
+
+// Packed sequences: chunk_base[n] = sum_{m < n} ceil(len_m / 64), n = 0..N.
+__global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ cu, int N,
+                                                        int* __restrict__ chunk_base) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int start = 0; start <= N; start += 1024) {
+    const int i = start + tid;
+    int cnt = 0;
+    if (i < N) {
+      const int len = cu[i + 1] - cu[i];
+      if (len < 0) set_status(1);
+      cnt = len > 0 ? (len + CH - 1) / CH : 0;
+    }
+    int x = cnt;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int t = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      warp_tot[lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry_s + (w > 0 ? warp_tot[w - 1] : 0) + x - cnt;
+    if (i <= N) chunk_base[i] = excl;
+    __syncthreads();
+    if (tid == 0) carry_s += warp_tot[31];
+    __syncthreads();
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, uint32_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 template <int DIN, typename OutT>
-cudaError_t launch_variant(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& tg, const Params& prm,
-                           cudaStream_t stream) {
-  auto kern = kda_chunk_kernel<DIN, OutT>;
+cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tg, int* chunk_base,
+                          uint8_t* records, int grid_chunks, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    cudaError_t e = set_smem(kda_intra_kernel<DIN>, A_SMEM);
+    if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((unsigned)pr.H, (unsigned)pr.n_seq);
-  kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tg, prm);
+  IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
+                 pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0};
+  kda_intra_kernel<DIN><<<dim3((unsigned)grid_chunks, (unsigned)pr.H), 128, A_SMEM, stream>>>(
+      tq, tk, tg, ip);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  StateParams sp{records, pr.initial_state, pr.final_state, pr.out, pr.cu_seqlens, chunk_base,
+                 pr.T, pr.n_seq, pr.H, pr.scale};
+  kda_state_kernel<DIN, OutT><<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), 128, B_SMEM, stream>>>(
+      tv, sp);
   return cudaGetLastError();
 }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 }  // namespace
 
-cudaError_t launch_chunk_fwd(const ChunkProblem& pr, cudaStream_t stream) {
+size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H) {
+  long long chunks;
+  size_t plan = 0;
+  if (packed) {
+    chunks = T_or_total / CH + n_seq;  // sum of ceil(len / 64) is at most this
+    plan = align_up((size_t)(n_seq + 1) * sizeof(int), 1024);
+  } else {
+    chunks = (long long)n_seq * ((T_or_total + CH - 1) / CH);
+  }
+  return plan + (size_t)chunks * H * REC_BYTES;
+}
+
+cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream_t stream) {
   const uint64_t d = (uint64_t)pr.d, H = (uint64_t)pr.H;
   if (pr.T_total == 0) {
     // no tokens at all: the final state is the initial state
@@ -650,6 +895,21 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& pr, cudaStream_t stream) {
                                    cudaMemcpyDeviceToDevice, stream);
     return cudaMemsetAsync(pr.final_state, 0, bytes, stream);
   }
+  const bool packed = pr.cu_seqlens != nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* chunk_base = nullptr;
+  int grid_chunks;
+  if (packed) {
+    chunk_base = reinterpret_cast<int*>(ws);
+    ws += align_up((size_t)(pr.n_seq + 1) * sizeof(int), 1024);
+    kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, chunk_base);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    grid_chunks = pr.T_total / CH + pr.n_seq;
+  } else {
+    grid_chunks = pr.n_seq * ((pr.T + CH - 1) / CH);
+  }
+  if (grid_chunks == 0) return cudaSuccess;
   const uint64_t rows = (uint64_t)pr.T_total;
   CUtensorMap tq, tk, tv, tg;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -658,13 +918,13 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& pr, cudaStream_t stream) {
       !make_map_3d_bf16(&tv, pr.v, d, H, rows, d, H * d, 64, 1, 64, sw) ||
       !make_map_3d_bf16(&tg, pr.log_alpha, d, H, rows, d, H * d, 64, 1, 64, sw))
     return cudaErrorInvalidValue;
-  Params prm{static_cast<const __nv_bfloat16*>(pr.beta), pr.initial_state, pr.out,
-             pr.final_state, pr.cu_seqlens, pr.T, pr.H, pr.scale, pr.check_decay ? 1 : 0};
   if (pr.d == 128)
-    return pr.out_f32 ? launch_variant<128, float>(pr, tq, tk, tv, tg, prm, stream)
-                      : launch_variant<128, __nv_bfloat16>(pr, tq, tk, tv, tg, prm, stream);
-  return pr.out_f32 ? launch_variant<64, float>(pr, tq, tk, tv, tg, prm, stream)
-                    : launch_variant<64, __nv_bfloat16>(pr, tq, tk, tv, tg, prm, stream);
+    return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, chunk_base, ws, grid_chunks, stream)
+                      : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, ws,
+                                                          grid_chunks, stream);
+  return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, ws, grid_chunks, stream)
+                    : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, ws,
+                                                       grid_chunks, stream);
 }
 
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err) {

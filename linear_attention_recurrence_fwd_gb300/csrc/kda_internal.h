@@ -32,7 +32,11 @@ struct ChunkProblem {
   bool check_decay;
 };
 
-cudaError_t launch_chunk_fwd(const ChunkProblem& p, cudaStream_t stream);
+// Device workspace the chunked prefill needs: per-(chunk, head) records
+// (and, for packed sequences, the per-sequence chunk offsets).
+size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H);
+
+cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 
 // Device status word of the chunk kernels (0 = ok, else a kda_status_t).
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err);

@@ -18,25 +18,27 @@ struct ProbeArgs {
   int a_mn, a_sw, a_mn_blocks_contig;
   int b_mn, b_sw, b_mn_blocks_contig;
   int b_row0, neg_a, n_accum;
+  int tf32;  // operands are fp32, MMA kind::tf32
 };
 
 constexpr int kProbeSmem = 1024 + 32 * 1024 + 64 * 1024 + 1024;
 
 __host__ __device__ OperandLayout probe_layout(uint32_t base, int rows, int K, int mn, int sw,
-                                               int blocks_contig) {
+                                               int blocks_contig, uint32_t esize) {
   OperandLayout L;
   L.base = base;
+  L.esize = esize;
   L.sw = (uint32_t)sw;
   L.mn_major = mn != 0;
   const uint32_t S = swizzle_bytes(L.sw);
-  const uint32_t W = S / 2;
+  const uint32_t W = S / esize;
   if (!L.mn_major) {
     L.sbo = 8 * S;
     L.kb_stride = (uint32_t)rows * S;
     L.lbo = 0;
   } else if (!blocks_contig) {  // the K groups of one MN block are contiguous
     L.sbo = 8 * S;
-    L.lbo = (uint32_t)K * S;
+    L.lbo = (uint32_t)K * S;  // K rows of S bytes per MN block
     L.kb_stride = 0;
   } else {  // the MN blocks of one K group are contiguous
     L.lbo = 8 * S;
@@ -58,18 +60,25 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
   const uint32_t b_base = a_base + 32 * 1024;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
-  const OperandLayout LA = probe_layout(a_base, p.M, p.K, p.a_mn, p.a_sw, p.a_mn_blocks_contig);
-  const OperandLayout LB = probe_layout(b_base, p.NB, p.K, p.b_mn, p.b_sw, p.b_mn_blocks_contig);
+  const uint32_t es = p.tf32 ? 4u : 2u;
+  const OperandLayout LA = probe_layout(a_base, p.M, p.K, p.a_mn, p.a_sw, p.a_mn_blocks_contig, es);
+  const OperandLayout LB = probe_layout(b_base, p.NB, p.K, p.b_mn, p.b_sw, p.b_mn_blocks_contig, es);
   // zero both regions, then scatter the logical matrices into them
   for (uint32_t off = tid * 16; off < 96 * 1024; off += 128 * 16) st_shared_v4(a_base + off, 0, 0, 0, 0);
   __syncthreads();
   for (int idx = tid; idx < p.M * p.K; idx += 128) {
     const int r = idx / p.K, k = idx % p.K;
-    st_shared_u16(layout_addr(LA, r, k), __bfloat16_as_ushort(A[idx]));
+    if (p.tf32)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(layout_addr(LA, r, k)), "f"(__bfloat162float(A[idx])));
+    else
+      st_shared_u16(layout_addr(LA, r, k), __bfloat16_as_ushort(A[idx]));
   }
   for (int idx = tid; idx < p.NB * p.K; idx += 128) {
     const int r = idx / p.K, k = idx % p.K;
-    st_shared_u16(layout_addr(LB, r, k), __bfloat16_as_ushort(B[idx]));
+    if (p.tf32)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(layout_addr(LB, r, k)), "f"(__bfloat162float(B[idx])));
+    else
+      st_shared_u16(layout_addr(LB, r, k), __bfloat16_as_ushort(B[idx]));
   }
   fence_proxy_async_smem();
   if (tid == 0) {
@@ -86,11 +95,19 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
   const uint32_t tbase = tmem_base_s;
 
   if (tid == 0) {
-    const uint32_t idesc = make_idesc_bf16(p.M, p.N, p.a_mn != 0, p.b_mn != 0, p.neg_a != 0);
-    for (int rep = 0; rep < p.n_accum; ++rep)
-      for (int k0 = 0; k0 < p.K; k0 += 16)
-        umma_bf16(tbase, layout_desc(LA, 0, k0), layout_desc(LB, p.b_row0, k0), idesc,
-                  (rep > 0 || k0 > 0) ? 1u : 0u);
+    if (p.tf32) {
+      const uint32_t idesc = make_idesc_tf32(p.M, p.N, p.a_mn != 0, p.b_mn != 0);
+      for (int rep = 0; rep < p.n_accum; ++rep)
+        for (int k0 = 0; k0 < p.K; k0 += 8)
+          umma_tf32(tbase, layout_desc(LA, 0, k0), layout_desc(LB, p.b_row0, k0), idesc,
+                    (rep > 0 || k0 > 0) ? 1u : 0u);
+    } else {
+      const uint32_t idesc = make_idesc_bf16(p.M, p.N, p.a_mn != 0, p.b_mn != 0, p.neg_a != 0);
+      for (int rep = 0; rep < p.n_accum; ++rep)
+        for (int k0 = 0; k0 < p.K; k0 += 16)
+          umma_bf16(tbase, layout_desc(LA, 0, k0), layout_desc(LB, p.b_row0, k0), idesc,
+                    (rep > 0 || k0 > 0) ? 1u : 0u);
+    }
     umma_commit(&bar);
   }
   const bool ok = mbar_wait(&bar, 0);
@@ -152,12 +169,13 @@ __global__ void __launch_bounds__(128) probe_tma_kernel(const __grid_constant__ 
 extern "C" KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N, int K, int NB,
                               int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
                               int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum,
-                              int* status, cudaStream_t stream) {
+                              int tf32, int* status, cudaStream_t stream) {
   if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K % 16 || K > 128 || K < 16)
     return 1;
   if (NB < b_row0 + N || NB > 256 || (a_mn && M % 64) || n_accum < 1) return 1;
+  if (tf32 && (neg_a || (size_t)NB * K * 4 > 64 * 1024 || (size_t)M * K * 4 > 32 * 1024)) return 1;
   ProbeArgs p{M, N, K, NB, a_mn, a_sw, a_mn_blocks_contig, b_mn, b_sw, b_mn_blocks_contig,
-              b_row0, neg_a, n_accum};
+              b_row0, neg_a, n_accum, tf32};
   if (cudaFuncSetAttribute(probe_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kProbeSmem) != cudaSuccess)
     return 4;

@@ -168,6 +168,22 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
   return make_idesc(M, N, a_mn_major, b_mn_major, negate_a, false);
 }
 
+// kind::tf32: fp32 operands read as tf32 (10-bit mantissa, fp32 range), K = 8 per MMA.
+__host__ __device__ constexpr uint32_t make_idesc_tf32(int M, int N, bool a_mn_major,
+                                                       bool b_mn_major) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -199,6 +215,7 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // are LBO apart, groups of 8 K-rows are SBO apart.
 struct OperandLayout {
   uint32_t base;       // smem byte address of the tile (aligned to 8*S)
+  uint32_t esize = 2;  // element bytes (2: bf16/fp16, 4: tf32)
   uint32_t sw;         // Swizzle code
   bool mn_major;
   uint32_t lbo;        // MN-major: stride between MN blocks
@@ -210,11 +227,11 @@ struct OperandLayout {
 __host__ __device__ __forceinline__ uint32_t layout_offset(const OperandLayout& L, uint32_t row,
                                                            uint32_t k) {
   const uint32_t S = swizzle_bytes(L.sw);
-  const uint32_t W = S / 2;  // elements per atom row
+  const uint32_t W = S / L.esize;  // elements per atom row
   if (!L.mn_major) {
-    return (k / W) * L.kb_stride + (row / 8) * L.sbo + (row % 8) * S + (k % W) * 2;
+    return (k / W) * L.kb_stride + (row / 8) * L.sbo + (row % 8) * S + (k % W) * L.esize;
   }
-  return (row / W) * L.lbo + (k / 8) * L.sbo + (k % 8) * S + (row % W) * 2;
+  return (row / W) * L.lbo + (k / 8) * L.sbo + (k % 8) * S + (row % W) * L.esize;
 }
 
 // Apply the XOR swizzle (16-byte chunk index ^= 128-byte line index, masked
@@ -230,7 +247,7 @@ __host__ __device__ __forceinline__ uint32_t layout_addr(const OperandLayout& L,
   return swizzle_addr(L.base + layout_offset(L, row, k), L.sw);
 }
 
-// Descriptor for the 16-wide K slice starting at k0 (k0 % 16 == 0), rows
+// Descriptor for the K slice starting at k0 (16 wide for 16-bit types, 8 for tf32), rows
 // starting at row0 (row0 % 8 == 0 for K-major; MN-major row0 may point
 // inside an atom row, which moves the start address by row0*2 bytes).
 __device__ __forceinline__ uint64_t layout_desc(const OperandLayout& L, uint32_t row0,
@@ -250,6 +267,33 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Untiled bulk copies (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_global, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(src_global)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst_global, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst_global)),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk store has finished (reads and writes).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_reads() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- misc

@@ -20,7 +20,7 @@ def probe(cuda_device):
 
 
 def _run(probe, M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0=0, NB=None, neg=0, acc=1,
-         seed=0):
+         seed=0, tf32=0):
     NB = NB or (b_row0 + N)
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, K, generator=g).bfloat16()
@@ -29,7 +29,7 @@ def _run(probe, M, N, K, a_mn, a_sw, a_bc, b_mn, b_sw, b_bc, b_row0=0, NB=None, 
     D = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = probe.kda_probe_umma(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, NB, a_mn, a_sw,
-                              a_bc, b_mn, b_sw, b_bc, b_row0, neg, acc, st.data_ptr(),
+                              a_bc, b_mn, b_sw, b_bc, b_row0, neg, acc, tf32, st.data_ptr(),
                               torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
@@ -100,3 +100,21 @@ def test_tma_tile_matches_layout(probe, d, t0):
     n = min(64, T - t0)
     exp[:n] = src[t0:t0 + n, h].cpu()
     assert torch.equal(out.cpu(), exp)
+
+
+# Only K-major operands: with MN-major fp32 operands (laid out like the 16-bit
+# MN-major atoms, 32 fp32 per 128-byte row) kind::tf32 did not reproduce the
+# matmul on GB300, so the kernels keep tf32 out of the MN-major products.
+TF32_CASES = [
+    # M, N, K, a_mn, a_sw, b_mn, b_sw, b_row0, NB
+    (128, 64, 32, 0, SW128, 0, SW128, 0, None),
+    (128, 64, 64, 0, SW128, 0, SW128, 0, None),
+]
+
+
+@pytest.mark.parametrize("case", TF32_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_umma_tf32_layouts(probe, case):
+    """kind::tf32 with fp32 operands (bf16-valued inputs, so products are exact)."""
+    M, N, K, a_mn, a_sw, b_mn, b_sw, b_row0, NB = case
+    D, exp = _run(probe, M, N, K, a_mn, a_sw, 0, b_mn, b_sw, 0, b_row0, NB, tf32=1)
+    assert _close(D, exp), f"max err {(D - exp).abs().max().item():.3e}"
