@@ -87,6 +87,7 @@ constexpr uint32_t A_STG = 0;                             // record image [0, 64
 constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][64]  (after M1)
 constexpr uint32_t A_KT = 81920;                          // (k e^g)^T bf16      (after M1)
 constexpr uint32_t A_TI = 0;                              // T fp32 (in the W slot, before W)
+constexpr uint32_t A_DINV = 57344;                        // T_aa transposed, 4 KB (in the T diag(beta) slot, before it)
 constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
 constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
 
@@ -99,7 +100,7 @@ constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
 constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
-constexpr uint32_t TB_U = 0, TB_O = 64, TB_S = 128, TB_COLS = 256;
+constexpr uint32_t TB_U = 0, TB_O = 64, TB_S = 256, TB_COLS = 512;  // O: two 64-col buffers
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -143,16 +144,18 @@ __device__ __forceinline__ void st8h(uint32_t addr, const float* x) {
   st_shared_v4(addr, pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
                pack_f16x2(x[6], x[7]));
 }
-// x as an unevaluated bf16 pair: hi = bf16(x), lo = bf16(x - hi).
+// x as an unevaluated bf16 pair: hi = bf16(x), lo = bf16(x - hi).  Each
+// packed hi pair is widened back with bit operations (bf16 -> fp32 is exact).
 __device__ __forceinline__ void st8_split(uint32_t addr_hi, uint32_t addr_lo, const float* x) {
-  float hi[8], lo[8];
+  uint32_t hi[4], lo[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    hi[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
-    lo[j] = x[j] - hi[j];
+  for (int j = 0; j < 4; ++j) {
+    hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+    const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
+    lo[j] = pack_bf16x2(x[2 * j] - h0, x[2 * j + 1] - h1);
   }
-  st8(addr_hi, hi);
-  st8(addr_lo, lo);
+  st_shared_v4(addr_hi, hi[0], hi[1], hi[2], hi[3]);
+  st_shared_v4(addr_lo, lo[0], lo[1], lo[2], lo[3]);
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -238,6 +241,58 @@ __device__ __forceinline__ void build_version(const OperandLayout& XH, const Ope
   }
 }
 
+// T (fp32 64x64) with 16-byte chunks XOR-swizzled by row.
+__device__ __forceinline__ int tix(int r, int c) {
+  return r * CH + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
+}
+
+// Off-diagonal blocks at distance S: T_ab = -T_aa sum_{m=b}^{a-1} L_am T_mb
+// for a - b = S.  akk holds L transposed (akk[i][r] = L[r][i]); dinv[a][x][rr]
+// = T_aa[rr][x]; P goes to the unused upper-triangle block (b, a) of ti.
+template <int S>
+__device__ __forceinline__ void solve_level(const float* akk, float* ti, const float* dinv,
+                                            int tid) {
+  constexpr int kStrips = (4 - S) * 64;  // (block, row, 4-column quad)
+#pragma unroll
+  for (int st = tid; st < kStrips; st += 128) {
+    const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+    for (int mm = 0; mm < S; ++mm) {
+      const int m = b + mm;
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float l = akk[(16 * m + x) * CH + 16 * a + rr];
+        const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * m + x, 16 * b + 4 * q));
+        acc0 += l * t.x;
+        acc1 += l * t.y;
+        acc2 += l * t.z;
+        acc3 += l * t.w;
+      }
+    }
+    *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) =
+        make_float4(acc0, acc1, acc2, acc3);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int st = tid; st < kStrips; st += 128) {
+    const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const float d = dinv[(a * 16 + x) * 16 + rr];
+      const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * b + x, 16 * a + 4 * q));
+      acc0 += d * t.x;
+      acc1 += d * t.y;
+      acc2 += d * t.z;
+      acc3 += d * t.w;
+    }
+    *reinterpret_cast<float4*>(ti + tix(16 * a + rr, 16 * b + 4 * q)) =
+        make_float4(-acc0, -acc1, -acc2, -acc3);
+  }
+  __syncthreads();
+}
+
 struct IntraParams {
   const __nv_bfloat16* beta;
   uint8_t* records;
@@ -287,8 +342,8 @@ __global__ void __launch_bounds__(128, 2)
       st_shared_v4(sb + A_RG + 8192 + off, 0, 0, 0, 0);
     }
   }
-  if (tid < CH)
-    s_beta[tid] = tid < valid ? __bfloat162float(p.beta[(size_t)(loc.t0 + tid) * H + h]) : 0.f;
+  const float beta_t =
+      tid < valid ? __bfloat162float(p.beta[(size_t)(loc.t0 + tid) * H + h]) : 0.f;
   // L[r][i] = (i <= r), I[r][i] = (i == r), both restricted to valid tokens i
   const OperandLayout LM = kmajor(sb + A_LM, 0), IM = kmajor(sb + A_IM, 0);
   {
@@ -306,6 +361,7 @@ __global__ void __launch_bounds__(128, 2)
       st8(layout_addr(IM, r, i0), e);
     }
   }
+  if (tid < CH) s_beta[tid] = beta_t;
   if (warp == 0) {
     tmem_alloc(tmem_base_s, TA_COLS);
     tmem_relinquish();
@@ -349,13 +405,16 @@ __global__ void __launch_bounds__(128, 2)
   }
   constexpr uint32_t ID_T = make_idesc(128, 64, true, false);  // bf16, A MN-major
   if (ok && tid == 0) {
-    const OperandLayout RQ = mnmajor(sb + A_RQ, 8192), RK = mnmajor(sb + A_RK, 8192);
-    const OperandLayout RG = mnmajor(sb + A_RG, 8192);
+    const uint64_t dq = layout_desc(mnmajor(sb + A_RQ, 8192), 0, 0);
+    const uint64_t dk = layout_desc(mnmajor(sb + A_RK, 8192), 0, 0);
+    const uint64_t dg = layout_desc(mnmajor(sb + A_RG, 8192), 0, 0);
+    const uint64_t dl = layout_desc(LM, 0, 0), di = layout_desc(IM, 0, 0);
 #pragma unroll
     for (int k0 = 0; k0 < CH; k0 += 16) {
-      umma_bf16(tmem + TA_G, layout_desc(RG, 0, k0), layout_desc(LM, 0, k0), ID_T, k0 > 0);
-      umma_bf16(tmem + TA_Q, layout_desc(RQ, 0, k0), layout_desc(IM, 0, k0), ID_T, k0 > 0);
-      umma_bf16(tmem + TA_K, layout_desc(RK, 0, k0), layout_desc(IM, 0, k0), ID_T, k0 > 0);
+      const uint64_t bl = desc_adv(dl, k0, false), bi = desc_adv(di, k0, false);
+      umma_bf16(tmem + TA_G, desc_adv(dg, k0, true), bl, ID_T, k0 > 0);
+      umma_bf16(tmem + TA_Q, desc_adv(dq, k0, true), bi, ID_T, k0 > 0);
+      umma_bf16(tmem + TA_K, desc_adv(dk, k0, true), bi, ID_T, k0 > 0);
     }
     umma_commit(bar_mma);
   }
@@ -409,11 +468,14 @@ __global__ void __launch_bounds__(128, 2)
     operands_ready();
     if (tid == 0) {
       const uint32_t d = tmem + TA_A + 16 * b;
+      const uint64_t xh = layout_desc(XH, 0, 0), xl = layout_desc(XL, 0, 0);
+      const uint64_t bh = layout_desc(KBH, 16 * b, 0), bl = layout_desc(KBL, 16 * b, 0);
 #pragma unroll
       for (int k0 = 0; k0 < DP; k0 += 16) {
-        umma_bf16(d, layout_desc(XH, 0, k0), layout_desc(KBH, 16 * b, k0), ID_M1, k0 > 0);
-        umma_bf16(d, layout_desc(XL, 0, k0), layout_desc(KBH, 16 * b, k0), ID_M1, 1);
-        umma_bf16(d, layout_desc(XH, 0, k0), layout_desc(KBL, 16 * b, k0), ID_M1, 1);
+        const uint64_t ah = desc_adv(xh, k0, true), bhk = desc_adv(bh, k0, true);
+        umma_bf16(d, ah, bhk, ID_M1, k0 > 0);
+        umma_bf16(d, desc_adv(xl, k0, true), bhk, ID_M1, 1);
+        umma_bf16(d, ah, desc_adv(bl, k0, true), ID_M1, 1);
       }
       umma_commit(bar_mma);
     }
@@ -442,19 +504,11 @@ __global__ void __launch_bounds__(128, 2)
           for (int j = 0; j < 8; ++j) x[j] = (i0 + j <= r) ? a[i0 + j] : 0.f;
           st8h(layout_addr(AQ, r, i0), x);
         }
-      } else {
+      } else {  // stored transposed, akk[i][r] = L[r][i]: the solve reads L by columns
         const int r = tid - CH;
         const float br = s_beta[r];
-        float4* row = reinterpret_cast<float4*>(akk + r * CH);
 #pragma unroll
-        for (int i0 = 0; i0 < CH; i0 += 4) {
-          float4 x;
-          x.x = (i0 + 0 < r) ? br * a[i0 + 0] : 0.f;
-          x.y = (i0 + 1 < r) ? br * a[i0 + 1] : 0.f;
-          x.z = (i0 + 2 < r) ? br * a[i0 + 2] : 0.f;
-          x.w = (i0 + 3 < r) ? br * a[i0 + 3] : 0.f;
-          row[i0 / 4] = x;
-        }
+        for (int i = 0; i < CH; ++i) akk[i * CH + r] = (i < r) ? br * a[i] : 0.f;
       }
     }
     // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
@@ -489,55 +543,47 @@ __global__ void __launch_bounds__(128, 2)
       bulk_commit();
     }
 
-    // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by forward substitution
+    // ---- T = (I + A_kk)^-1, unit lower triangular, in fp32.  L = I + A_kk is
+    // read transposed (akk[i][r] = L[r][i]); T lives in ti with its 16-byte
+    // chunks XOR-swizzled by row, so row-wise float4 traffic is conflict-free.
+    float* dinv = reinterpret_cast<float*>(sbp + A_DINV);  // [4][16][16], dinv[a][x][rr] = T_aa[rr][x]
+    // diagonal blocks by forward substitution: thread (a, j) solves column j of block a
     if (tid < 64) {
       const int a = tid >> 4, j = tid & 15;
       float x[16];
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) x[rr] = rr == j ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
+      for (int m = 0; m < 15; ++m) {
         const float xm = x[m];
 #pragma unroll
-        for (int rr = m + 1; rr < 16; ++rr) x[rr] -= akk[(16 * a + rr) * CH + 16 * a + m] * xm;
+        for (int rr = m + 1; rr < 16; ++rr) x[rr] -= akk[(16 * a + m) * CH + 16 * a + rr] * xm;
       }
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) ti[(16 * a + rr) * CH + 16 * a + j] = x[rr];
+      for (int rr = 0; rr < 16; ++rr) ti[tix(16 * a + rr, 16 * a + j)] = x[rr];
+      float4* drow = reinterpret_cast<float4*>(dinv + (a * 16 + j) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) drow[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
     __syncthreads();
-    // ---- off-diagonal blocks: T_ab = -T_aa sum_{m=b}^{a-1} L_am T_mb, by distance a - b
-#pragma unroll 1
-    for (int s = 1; s < 4; ++s) {
-      const int nel = (4 - s) * 256;
-      for (int e = tid; e < nel; e += 128) {
-        const int b = e >> 8, a = b + s, rr = (e >> 4) & 15, cc = e & 15;
-        float acc = 0.f;
-        for (int m = b; m < a; ++m)
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            acc += akk[(16 * a + rr) * CH + 16 * m + x] * ti[(16 * m + x) * CH + 16 * b + cc];
-        ti[(16 * b + rr) * CH + 16 * a + cc] = acc;  // scratch in the (zero) upper triangle
-      }
-      __syncthreads();
-      for (int e = tid; e < nel; e += 128) {
-        const int b = e >> 8, a = b + s, rr = (e >> 4) & 15, cc = e & 15;
-        float acc = 0.f;
-        for (int x = 0; x <= rr; ++x)
-          acc += ti[(16 * a + rr) * CH + 16 * a + x] * ti[(16 * b + x) * CH + 16 * a + cc];
-        ti[(16 * a + rr) * CH + 16 * b + cc] = -acc;
-      }
-      __syncthreads();
-    }
+    // off-diagonal blocks by distance s = a - b: P = sum_{m=b}^{a-1} L_am T_mb,
+    // then T_ab = -T_aa P.  A thread owns a strip of 4 columns of one row.
+    solve_level<1>(akk, ti, dinv, tid);
+    solve_level<2>(akk, ti, dinv, tid);
+    solve_level<3>(akk, ti, dinv, tid);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
       const int r = tid >> 1, i_lo = (tid & 1) * 32;
 #pragma unroll
       for (int i0 = i_lo; i0 < i_lo + 32; i0 += 8) {
+        const float4 t0 = *reinterpret_cast<const float4*>(ti + tix(r, i0));
+        const float4 t1 = *reinterpret_cast<const float4*>(ti + tix(r, i0 + 4));
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
         float x[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int i = i0 + j;
-          x[j] = i <= r ? ti[r * CH + i] * s_beta[i] : 0.f;
+          x[j] = i <= r ? tv[j] * s_beta[i] : 0.f;
         }
         st8(layout_addr(TB, r, i0), x);
       }
@@ -545,9 +591,10 @@ __global__ void __launch_bounds__(128, 2)
     operands_ready();
     if (tid == 0) {
       constexpr uint32_t ID_W = make_idesc(128, 64, false, false);
+      const uint64_t dkt = layout_desc(KT, 0, 0), dtb = layout_desc(TB, 0, 0);
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16)
-        umma_bf16(tmem + TA_W, layout_desc(KT, 0, k0), layout_desc(TB, 0, k0), ID_W, k0 > 0);
+        umma_bf16(tmem + TA_W, desc_adv(dkt, k0, false), desc_adv(dtb, k0, false), ID_W, k0 > 0);
       umma_commit(bar_mma);
     }
     ok = wait_all(bar_mma, mma_phase);
@@ -584,19 +631,31 @@ struct StateParams {
   float scale;
 };
 
+// Stage 2 warp roles: warps 0-7 run the serial chain (two per TMEM lane
+// quadrant, splitting columns); warps 8-11 drain finished output tiles from
+// TMEM to global memory, double-buffered, off the chain.
+constexpr int B_CHAIN = 256;
+constexpr int B_THREADS = 384;
+
+__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 template <int DIN, typename OutT>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(B_THREADS, 1)
     kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int half = (warp >> 2) & 1;           // chain warps: which half of the columns
+  const int v = 32 * (warp & 3) + (tid & 31);  // TMEM lane = value channel
   const int h = blockIdx.x, n = blockIdx.y, H = p.H;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sbp = smem_raw + (sb - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sbp + B_MISC);  // [2]
-  uint64_t* bar_mma = full + 2;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 32);
-  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 36);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbp + B_MISC);  // [2] record + v tile landed
+  uint64_t* bar_mma = full + 2;                                // chain MMAs done
+  uint64_t* o_full = full + 3;                                 // [2] output tile ready
+  uint64_t* o_empty = full + 5;                                // [2] output tile drained
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 64);
+  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 68);
 
   int tok0, len, base;
   if (p.cu) {
@@ -621,18 +680,25 @@ __global__ void __launch_bounds__(128, 1)
     for (int b = 0; b < DIN / 64; ++b)
       tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * j);
   };
+  auto gamma_of = [&](int buf) {
+    return reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
+  };
 
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
     mbar_init(bar_mma, 1);
+    mbar_init(&o_full[0], 1);
+    mbar_init(&o_full[1], 1);
+    mbar_init(&o_empty[0], B_THREADS - B_CHAIN);
+    mbar_init(&o_empty[1], B_THREADS - B_CHAIN);
     mbar_fence_init();
     *s_abort = 0;
     if (nchunks > 0) issue_loads(0, 0);
     if (nchunks > 1) issue_loads(1, 1);
   }
   if (DIN == 64) {
-    for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
+    for (uint32_t off = tid * 16; off < 8192; off += B_THREADS * 16) {
       st_shared_v4(sb + B_V0 + 8192 + off, 0, 0, 0, 0);
       st_shared_v4(sb + B_V1 + 8192 + off, 0, 0, 0, 0);
     }
@@ -645,117 +711,22 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_s;
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-  const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
-  const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
+  const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 
-  // initial state: thread v holds row v of S^T
-  const int v = tid;
-  const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
-#pragma unroll
-  for (int c0 = 0; c0 < DP; c0 += 16) {
-    float s[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int c = c0 + j;
-      s[j] = (p.s0 && c < DIN && v < DIN) ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
-    }
-    tmem_st16(tl + TB_S + c0, s);
-    st8h(layout_addr(ST, v, c0), s);
-    st8h(layout_addr(ST, v, c0 + 8), s + 8);
-  }
-  tmem_st_wait();
-
-  auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
-    if (!mbar_wait(bar, phase)) {
-      *s_abort = 1;
-      set_status(6);
-    }
-    __syncthreads();
-    tc_fence_after_sync();
-    return *s_abort == 0;
-  };
-  auto operands_ready = [&]() {
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-  };
-  operands_ready();
-
-  constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
-  constexpr uint32_t ID_U = make_idesc(128, 64, false, true, true, true);     // fp16, -A
-  constexpr uint32_t ID_O1 = make_idesc(128, 64, false, true, false, true);   // fp16
-  constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, false, true);  // fp16
-  constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  int pending = min(nchunks, 2);  // record loads in flight
-
-  for (int j = 0; j < nchunks && ok; ++j) {
-    const int buf = j & 1;
-    const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
-    const uint32_t vb = sb + (buf ? B_V1 : B_V0);
-    const float* gam = reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
-    const int valid = min(CH, len - CH * j);
-    if (!(ok = wait_all(&full[buf], (j >> 1) & 1))) break;
-    --pending;
-    const OperandLayout VA = mnmajor(vb, 8192);
-    const OperandLayout TB = kmajor(rb + REC_TB, 0), WT = mnmajor(rb + REC_WT, 16384);
-    const OperandLayout QT = mnmajor(rb + REC_QT, 16384), AQ = kmajor(rb + REC_AQ, 0);
-    const OperandLayout KBAR = kmajor(rb + REC_KBAR, 0);
-    if (tid == 0) {
-#pragma unroll
-      for (int k0 = 0; k0 < CH; k0 += 16)
-        umma_bf16(tmem + TB_U, layout_desc(VA, 0, k0), layout_desc(TB, 0, k0), ID_V, k0 > 0);
-#pragma unroll
-      for (int k0 = 0; k0 < DP; k0 += 16) {
-        umma_bf16(tmem + TB_U, layout_desc(ST, 0, k0), layout_desc(WT, 0, k0), ID_U, 1);
-        umma_bf16(tmem + TB_O, layout_desc(ST, 0, k0), layout_desc(QT, 0, k0), ID_O1, k0 > 0);
+  if (tid >= B_CHAIN) {
+    // ---------------- output warps: thread = value channel v, all 64 tokens
+    for (int j = 0; j < nchunks; ++j) {
+      const int ob = j & 1;
+      if (!mbar_wait(&o_full[ob], (j >> 1) & 1)) {
+        set_status(6);
+        break;
       }
-      umma_commit(bar_mma);
-    }
-    // decay the fp32 state by e^{g_C} while the tensor core works on U and O
-#pragma unroll
-    for (int c0 = 0; c0 < DP; c0 += 16) {
-      float s[16];
-      tmem_ld16(tl + TB_S + c0, s);
-      tmem_ld_wait();
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) s[jj] *= gam[c0 + jj];
-      tmem_st16(tl + TB_S + c0, s);
-    }
-    tmem_st_wait();
-    if (!(ok = wait_all(bar_mma, mma_phase))) break;
-    mma_phase ^= 1u;
-    {
-      float u[64];
-      tmem_ld64(tl + TB_U, u);
-#pragma unroll
-      for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(UT, v, r0), u + r0);
-    }
-    operands_ready();
-    if (tid == 0) {
-#pragma unroll
-      for (int k0 = 0; k0 < CH; k0 += 16) {
-        umma_bf16(tmem + TB_O, layout_desc(UT, 0, k0), layout_desc(AQ, 0, k0), ID_O2, 1);
-        umma_bf16(tmem + TB_S, layout_desc(UT, 0, k0), layout_desc(KBAR, 0, k0), ID_S, 1);
-      }
-      umma_commit(bar_mma);
-    }
-    if (!(ok = wait_all(bar_mma, mma_phase))) break;
-    mma_phase ^= 1u;
-    if (j + 2 < nchunks) {  // this buffer is consumed: fetch chunk j + 2 into it
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        issue_loads(j + 2, buf);
-      }
-      ++pending;
-    }
-    // outputs, and the fp16 state operand for the next chunk
-    {
+      tc_fence_after_sync();
+      const int valid = min(CH, len - CH * j);
       float o[64];
-      tmem_ld64(tl + TB_O, o);
+      tmem_ld64(tl + TB_O + 64 * ob, o);
+      tc_fence_before_sync();
+      mbar_arrive(&o_empty[ob]);  // the TMEM tile may be overwritten now
       if (v < DIN) {
         OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * j) * H * DIN +
                     (size_t)h * DIN + v;
@@ -763,32 +734,156 @@ __global__ void __launch_bounds__(128, 1)
         for (int r = 0; r < CH; ++r)
           if (r < valid) store_out(out + (size_t)r * H * DIN, p.scale * o[r]);
       }
+    }
+  } else {
+    // ---------------- chain warps
+    const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
+    const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
+    auto wait_chain = [&](uint64_t* bar, uint32_t phase) -> bool {
+      if (!mbar_wait(bar, phase)) {
+        *s_abort = 1;
+        set_status(6);
+      }
+      chain_sync();
+      tc_fence_after_sync();
+      return *s_abort == 0;
+    };
+    auto operands_ready = [&]() {
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      chain_sync();
+      tc_fence_after_sync();
+    };
+
+    bool ok = true;
+    int pending = min(nchunks, 2);  // record loads in flight
+    if (nchunks > 0) {
+      ok = wait_chain(&full[0], 0);
+      if (ok) --pending;
+    }
+    // initial state: thread (v, half) holds S^T[v][64 half .. 64 half + 63]
+    const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+    const int c_lo = 64 * half;
 #pragma unroll
-      for (int c0 = 0; c0 < DP; c0 += 16) {
-        float s[16];
-        tmem_ld16(tl + TB_S + c0, s);
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      float s0[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int c = c_lo + c0 + jj;
+        s0[jj] = (p.s0 && c < DIN && v < DIN) ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
+      }
+      tmem_st16(tl + TB_S + c_lo + c0, s0);
+      st8h(layout_addr(ST, v, c_lo + c0), s0);
+      st8h(layout_addr(ST, v, c_lo + c0 + 8), s0 + 8);
+    }
+    tmem_st_wait();
+
+    constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
+    constexpr uint32_t ID_U = make_idesc(128, 64, false, true, true, true);     // fp16, -A
+    constexpr uint32_t ID_O1 = make_idesc(128, 64, false, true, false, true);   // fp16
+    constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, false, true);  // fp16
+    constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
+    uint32_t mma_phase = 0;
+
+    for (int j = 0; j < nchunks && ok; ++j) {
+      // invariant: record j is resident; ST = fp16(S_j); TMEM S = S_j (not yet decayed)
+      const int buf = j & 1, ob = j & 1;
+      const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
+      const uint32_t vb = sb + (buf ? B_V1 : B_V0);
+      const uint32_t to = tmem + TB_O + 64 * ob;
+      operands_ready();
+      if (tid == 0) {
+        if (j >= 2 && !mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1)) {
+          *s_abort = 1;
+          set_status(6);
+        }
+        const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
+        const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
+        const uint64_t dst = layout_desc(ST, 0, 0);
+        const uint64_t dwt = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
+        const uint64_t dqt = layout_desc(mnmajor(rb + REC_QT, 16384), 0, 0);
+        tc_fence_after_sync();
+#pragma unroll
+        for (int k0 = 0; k0 < CH; k0 += 16)
+          umma_bf16(tmem + TB_U, desc_adv(dva, k0, true), desc_adv(dtb, k0, false), ID_V, k0 > 0);
+#pragma unroll
+        for (int k0 = 0; k0 < DP; k0 += 16) {
+          const uint64_t a = desc_adv(dst, k0, false, 16384);
+          umma_bf16(tmem + TB_U, a, desc_adv(dwt, k0, true), ID_U, 1);
+          umma_bf16(to, a, desc_adv(dqt, k0, true), ID_O1, k0 > 0);
+        }
+        umma_commit(bar_mma);
+      }
+      {  // decay the fp32 state by this chunk's e^{g_C} while the tensor core runs
+        const float* gam = gamma_of(buf);
+        float sv[64];
+        tmem_ld64(tl + TB_S + 64 * half, sv);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float sd[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sd[jj] = sv[c0 + jj] * gam[64 * half + c0 + jj];
+          tmem_st16(tl + TB_S + 64 * half + c0, sd);
+        }
+        tmem_st_wait();
+      }
+      if (!(ok = wait_chain(bar_mma, mma_phase))) break;
+      mma_phase ^= 1u;
+      {  // U^T (fp16 operand): this thread's 32 tokens
+        float u[32];
+        tmem_ld16(tl + TB_U + 32 * half, *reinterpret_cast<float(*)[16]>(u));
+        tmem_ld16(tl + TB_U + 32 * half + 16, *reinterpret_cast<float(*)[16]>(u + 16));
         tmem_ld_wait();
-        st8h(layout_addr(ST, v, c0), s);
-        st8h(layout_addr(ST, v, c0 + 8), s + 8);
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
+      }
+      operands_ready();
+      if (tid == 0) {
+        const uint64_t dut = layout_desc(UT, 0, 0);
+        const uint64_t daq = layout_desc(kmajor(rb + REC_AQ, 0), 0, 0);
+        const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
+#pragma unroll
+        for (int k0 = 0; k0 < CH; k0 += 16) {
+          const uint64_t a = desc_adv(dut, k0, false);
+          umma_bf16(to, a, desc_adv(daq, k0, false), ID_O2, 1);
+          umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);
+        }
+        umma_commit(bar_mma);
+        umma_commit(&o_full[ob]);
+      }
+      if (!(ok = wait_chain(bar_mma, mma_phase))) break;
+      mma_phase ^= 1u;
+      const bool more = j + 1 < nchunks;
+      if (j + 2 < nchunks) {  // this buffer is consumed: fetch chunk j + 2 into it
+        if (tid == 0) {
+          fence_proxy_async_smem();
+          issue_loads(j + 2, buf);
+        }
+        ++pending;
+      }
+      {  // the fp16 state operand for the next chunk (and the final state)
+        float sv[64];
+        tmem_ld64(tl + TB_S + 64 * half, sv);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 8) st8h(layout_addr(ST, v, c_lo + c0), sv + c0);
+        if (!more && p.s1 && v < DIN) {  // final state S[c][v] = S^T[v][c]
+#pragma unroll
+          for (int c0 = 0; c0 < 64; ++c0)
+            if (c_lo + c0 < DIN) p.s1[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
+        }
+      }
+      if (more) {
+        if (!(ok = wait_chain(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
+        --pending;
       }
     }
-    operands_ready();
-  }
-
-  if (ok && p.s1) {  // final state from the fp32 accumulator: S[c][v] = S^T[v][c]
-#pragma unroll
-    for (int c0 = 0; c0 < DP; c0 += 16) {
-      float s[16];
-      tmem_ld16(tl + TB_S + c0, s);
-      tmem_ld_wait();
-      if (v < DIN)
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          if (c0 + jj < DIN) p.s1[sbase + (size_t)(c0 + jj) * DIN + v] = s[jj];
+    if (ok && nchunks == 0 && p.s1 && v < DIN) {  // no tokens: final state = initial state
+      for (int c = c_lo; c < c_lo + 64 && c < DIN; ++c)
+        p.s1[sbase + (size_t)c * DIN + v] = p.s0 ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
     }
-  }
-  if (!ok) {  // let copies already issued land before the CTA's memory goes away
-    for (int j = 0; j < 2 && pending > 0; ++j, --pending) mbar_wait(&full[j], 0, 100000000ull);
+    if (!ok && tid == 0) {  // let copies already issued land before the CTA's memory goes away
+      for (int j = 0; j < 2 && pending > 0; ++j, --pending) mbar_wait(&full[j], 0, 100000000ull);
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -861,8 +956,8 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   if (e != cudaSuccess) return e;
   StateParams sp{records, pr.initial_state, pr.final_state, pr.out, pr.cu_seqlens, chunk_base,
                  pr.T, pr.n_seq, pr.H, pr.scale};
-  kda_state_kernel<DIN, OutT><<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), 128, B_SMEM, stream>>>(
-      tv, sp);
+  kda_state_kernel<DIN, OutT>
+      <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
   return cudaGetLastError();
 }
 

@@ -256,6 +256,18 @@ __device__ __forceinline__ uint64_t layout_desc(const OperandLayout& L, uint32_t
   return make_sdesc(start, L.mn_major ? L.lbo : 16u, L.sbo, L.sw);
 }
 
+// Advance a 128B-swizzled 16-bit operand descriptor (built for K = 0) to the
+// K slice at k0.  MN-major: k0 / 8 groups of 8 K-rows, 1024 bytes apart;
+// K-major: k0 / 64 K-blocks kb_stride apart, plus 2 bytes per element inside
+// the 128-byte atom row.  With k0 a compile-time constant this folds to one
+// 64-bit add on the start-address field (addresses stay below 256 KiB).
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, int k0, bool mn_major,
+                                             uint32_t kb_stride = 0) {
+  const uint32_t bytes = mn_major ? (uint32_t)(k0 >> 3) * 1024u
+                                  : (uint32_t)(k0 >> 6) * kb_stride + (uint32_t)(k0 & 63) * 2u;
+  return d + (bytes >> 4);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {
