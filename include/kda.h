@@ -97,6 +97,33 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that are not allowed to
+ * allocate device memory at all: for example code whose device memory is
+ * budgeted up front by a serving runtime, or code running on a thread that
+ * must not call into an allocator.  (The pages have no counterpart; this is
+ * an interface convenience of this library.)
+ *
+ * Same arguments, layouts and results as kda_chunk_fwd, minus the workspace:
+ * the intermediate records go to a fixed 64 MiB device array inside the
+ * library instead.  Every GPU that loads the library holds that array until
+ * the process exits.  Limits and behaviour:
+ *   - B * ceil(T / 64) * H must be at most 1008 (one 65 KiB record per chunk
+ *     and head); larger problems return KDA_ERR_WORKSPACE before anything
+ *     is launched.  Use kda_chunk_fwd with a caller workspace for those.
+ *   - All calls share the array.  Calls whose work overlaps on the GPU (two
+ *     streams, or two host threads) race on it; serialise them.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current).  Make that first call before capturing
+ *     any CUDA graph that uses this entry point.
+ */
+KDA_API kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                           const void* log_alpha, const void* beta,
+                                           const float* initial_state, void* out,
+                                           kda_dtype_t out_dtype, float* final_state, int B,
+                                           int T, int H, int d_k, int d_v, float scale,
+                                           cudaStream_t stream);
+
+/*
  * kda_varlen_fwd -- chunked prefill of N packed sequences of unequal length.
  *   q, k, log_alpha : [T_total, H, d_k] bf16 (a leading batch of 1 is implied)
  *   v               : [T_total, H, d_v] bf16;   beta : [T_total, H] bf16

@@ -23,7 +23,8 @@ STATUS = {
     6: "device wait timed out", 7: "workspace too small",
 }
 
-EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_varlen_fwd",
+EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
+           "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
            "kda_last_device_status", "kda_version"]
 
@@ -51,6 +52,8 @@ def load(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         lib.kda_chunk_fwd.argtypes = [_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
         lib.kda_chunk_fwd.restype = _i
+        lib.kda_chunk_fwd_noalloc.argtypes = [_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _vp]
+        lib.kda_chunk_fwd_noalloc.restype = _i
         lib.kda_varlen_fwd.argtypes = [_vp] * 6 + [_i, _i, _i, _vp, _vp, _i, _vp, _i, _i, _i, _f,
                                                    _vp, _sz, _vp]
         lib.kda_varlen_fwd.restype = _i
@@ -133,6 +136,28 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
     _check(lib.kda_chunk_fwd(_p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state),
                              _p(out), _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv,
                              float(scale), _p(ws), ws_bytes, _stream(stream)), "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
+                          out_dtype=torch.float32, output_final_state=True, out=None,
+                          final_state=None, stream=None):
+    """kda_chunk_fwd without a workspace: the library's fixed device scratch is
+    used instead (B * ceil(T/64) * H <= 1008).  Outputs are allocated here
+    only when not passed in; pass `out` / `final_state` to allocate nothing."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(lib.kda_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+                                     _p(initial_state), _p(out), _dtype_code(out.dtype),
+                                     _p(final_state), B, T, H, dk, dv, float(scale),
+                                     _stream(stream)), "kda_chunk_fwd_noalloc")
     return out, final_state
 
 

@@ -90,6 +90,24 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
+kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                   const void* log_alpha, const void* beta,
+                                   const float* initial_state, void* out, kda_dtype_t out_dtype,
+                                   float* final_state, int B, int T, int H, int d_k, int d_v,
+                                   float scale, cudaStream_t stream) {
+  if (B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
+                                     final_state, H, d_k, d_v, (long long)B * T > 0);
+  if (st != KDA_OK) return st;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  const long long records = (long long)B * ((T + 63) / 64) * H;
+  if (records > (long long)kda::noalloc_max_records()) return KDA_ERR_WORKSPACE;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env()};
+  return from_cuda(kda::launch_chunk_fwd_noalloc(p, stream));
+}
+
 kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const void* log_alpha,
                             const void* beta, const int* cu_seqlens, int N, int T_total,
                             int max_seqlen, const float* initial_state, void* out,

@@ -54,6 +54,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kda_internal.h"
 #include "tma_host.h"
 #include "umma.cuh"
@@ -1020,6 +1022,42 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream
   return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, ws, grid_chunks, stream)
                     : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, ws,
                                                        grid_chunks, stream);
+}
+
+// ---- allocation-free variant --------------------------------------------
+// Scratch for kda_chunk_fwd_noalloc: a fixed 64 MiB device array that every
+// GPU loading this library holds until the process exits.  It holds up to
+// 1008 per-(chunk, head) records.  All calls share it and nothing in it has
+// to start at zero (every record is written before it is read); calls whose
+// work overlaps on the GPU race on it.
+namespace {
+constexpr size_t kNoAllocBytes = (size_t)64 << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+}  // namespace
+
+size_t noalloc_max_records() { return kNoAllocBytes / REC_BYTES; }
+
+cudaError_t launch_chunk_fwd_noalloc(const ChunkProblem& pr, cudaStream_t stream) {
+  // The array's device address, looked up once per device with that device
+  // current (in host code the symbol is only a host-side stand-in).
+  static std::mutex mu;
+  static void* addr[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  void* scratch;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      addr[dev] = ptr;
+    }
+    scratch = addr[dev];
+  }
+  return launch_chunk_fwd(pr, scratch, stream);
 }
 
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err) {

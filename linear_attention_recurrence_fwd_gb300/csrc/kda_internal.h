@@ -38,6 +38,11 @@ size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 
+// Same path with the library's fixed device scratch instead of a caller
+// workspace (fixed-length problems of at most noalloc_max_records() records).
+size_t noalloc_max_records();
+cudaError_t launch_chunk_fwd_noalloc(const ChunkProblem& p, cudaStream_t stream);
+
 // Device status word of the chunk kernels (0 = ok, else a kda_status_t).
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err);
 
