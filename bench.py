@@ -197,6 +197,81 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def time_call(fn, steps, warmup, stream):
+    """Average CUDA-event milliseconds of fn() over `steps` calls on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+# kernels one call launches: intra-chunk stage + state pass (+ the varlen plan)
+LAUNCHES_FIXED, LAUNCHES_VARLEN = 2, 3
+
+
+def extra_workloads(args, ws, dev, stream, x64, ms64):
+    """The other prefill shapes, timed the same way (inputs resident, larger
+    than L2), plus the per-pair diagonal ablation on the T = 65536 problem."""
+    from linear_attention_recurrence_fwd_gb300 import binding
+    from linear_attention_recurrence_fwd_gb300 import inputs as gen
+
+    res = {}
+    a64 = [x64[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    out = torch.empty(x64["v"].shape, dtype=torch.float32, device=dev)
+    fin = torch.empty_like(x64["initial_state"])
+
+    def ablation():
+        binding.kda_chunk_fwd(*a64, x64["initial_state"], out=out, final_state=fin)
+
+    os.environ["KDA_ABLATE_DIAG"] = "1"
+    try:
+        ms = reduce_max(time_call(ablation, 5, 3, stream), ws)
+    finally:
+        del os.environ["KDA_ABLATE_DIAG"]
+    tok = x64["q"].shape[0] * x64["q"].shape[1]
+    res["ablation_diag_per_pair"] = {
+        "workload": "prefill_64k with the diagonal tiles evaluated per position pair",
+        "ms": ms, "Mtok_s": ws * tok / ms / 1e3, "slowdown_vs_dense": ms / ms64, "steps": 5}
+    del out, fin, a64
+
+    def fixed(name, steps):
+        w = gen.WORKLOADS[name]
+        x = gen.workload_inputs(w, device=dev)
+        a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+        o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev)
+        f = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+        s0 = x["initial_state"] if w.init_std > 0 else None
+        ms = reduce_max(time_call(
+            lambda: binding.kda_chunk_fwd(*a, s0, out=o, final_state=f), steps, 3, stream), ws)
+        res[name] = {"workload": f"B={w.B} T={w.T} H={w.H} d={w.dk}", "ms": ms,
+                     "Mtok_s": ws * w.B * w.T / ms / 1e3, "steps": steps}
+
+    fixed("prefill_8k", 20)
+
+    w = gen.WORKLOADS["varlen_64k"]
+    x = gen.workload_inputs(w, device=dev)
+    cu = gen.cu_seqlens_of(w.seqlens).to(dev)
+    a = [x[k][0] for k in ("q", "k", "v", "log_alpha", "beta")]
+    o = torch.empty((w.T, w.H, w.dv), dtype=torch.float32, device=dev)
+    f = torch.empty((len(w.seqlens), w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    ms = reduce_max(time_call(lambda: binding.kda_varlen_fwd(
+        *a, cu, max(w.seqlens), None, out=o, final_state=f), 10, 3, stream), ws)
+    res["varlen_64k"] = {"workload": f"{len(w.seqlens)} packed sequences {list(w.seqlens)}, "
+                                     f"H={w.H} d={w.dk}",
+                         "ms": ms, "Mtok_s": ws * w.T / ms / 1e3, "steps": 10}
+    del x, a, o, f
+    torch.cuda.empty_cache()
+    fixed("long_1m", 3)
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_profile_case(local):
     """Small, fixed case for ncu captures (a few GB on the device at most)."""
     from linear_attention_recurrence_fwd_gb300 import binding
@@ -230,6 +305,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="time only the headline prefill and the decode step")
     ap.add_argument("--case", choices=["bench", "ncu"], default="bench",
                     help="ncu: only run the small profiling case (3 prefills at T=8192 "
                          "H=32, then 3 decode steps) and exit")
@@ -337,6 +414,12 @@ def main():
     e2e_ms_local = g0.elapsed_time(g1) / args.e2e_steps
     del dbuf, host
 
+    ms_max = reduce_max(ms_local, ws)
+    extra = None
+    if not args.skip_extra:
+        del out, fin
+        extra = extra_workloads(args, ws, dev, stream, x, ms_max)
+
     ms = reduce_max(ms_local, ws)
     dec_us = reduce_max(dec_us_local, ws)
     e2e_ms = reduce_max(e2e_ms_local, ws)
@@ -378,7 +461,9 @@ def main():
                    "steps": args.decode_steps, "workload": "256 seq x 32 heads x d128, fp32 out"},
         "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * LAUNCHES_FIXED,
+        "gpu_launches_note": f"{LAUNCHES_FIXED} per prefill call (intra-chunk stage, state pass)",
+        "workloads": extra,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

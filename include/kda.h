@@ -31,6 +31,12 @@
  *     scan it on the device and report a violation through
  *     kda_last_device_status(); without it, out-of-range values give
  *     unspecified results.
+ *   - With KDA_ABLATE_DIAG=1 in the environment (read on every call) the
+ *     prefill entry points evaluate the four diagonal 16x16 tiles of each
+ *     chunk per position pair in log space on CUDA cores, the evaluation
+ *     that needs no bound on the decay, instead of with the dense
+ *     tensor-core products.  Results agree within rounding; it exists to
+ *     measure what the bound saves.
  *   - Supported head dims: d_k = d_v = 128, and d_k = d_v = 64 (prefill
  *     only).  Others return KDA_ERR_UNSUPPORTED.
  *   - Base pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT), except

@@ -20,6 +20,13 @@ bool check_decay_env() {
   return cached == 1;
 }
 
+// Ablation switch, read on every call: KDA_ABLATE_DIAG=1 evaluates the
+// diagonal tiles per position pair instead of with the dense products.
+bool ablate_diag_env() {
+  const char* e = std::getenv("KDA_ABLATE_DIAG");
+  return e && e[0] && e[0] != '0';
+}
+
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 kda_status_t validate_prefill(const void* q, const void* k, const void* v, const void* la,
@@ -86,7 +93,8 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
   if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
-                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env()};
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(),
+                      ablate_diag_env()};
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
@@ -104,7 +112,8 @@ kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
   const long long records = (long long)B * ((T + 63) / 64) * H;
   if (records > (long long)kda::noalloc_max_records()) return KDA_ERR_WORKSPACE;
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
-                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env()};
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(),
+                      ablate_diag_env()};
   return from_cuda(kda::launch_chunk_fwd_noalloc(p, stream));
 }
 
@@ -126,7 +135,7 @@ kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const v
   if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
                       final_state, cu_seqlens, N, max_seqlen, T_total, H, d_k, scale,
-                      check_decay_env()};
+                      check_decay_env(), ablate_diag_env()};
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 

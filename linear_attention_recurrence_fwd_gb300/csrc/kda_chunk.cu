@@ -102,7 +102,10 @@ constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
 constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
-constexpr uint32_t TB_U = 0, TB_O = 64, TB_S = 256, TB_COLS = 512;  // O: two 64-col buffers
+// Stage 2: U~ (M3 result, two buffers), D = [-S^T W^T | -O^T] (two buffers of
+// 128 columns: the U correction and the output share one N = 128 product)
+// and the fp32 state S^T.
+constexpr uint32_t TB_UT = 0, TB_D = 128, TB_S = 384, TB_COLS = 512;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -295,6 +298,61 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
   __syncthreads();
 }
 
+// Ablation of the dense diagonal tiles: the four 16x16 diagonal tiles of
+// A_qk and A_kk evaluated per position pair in log space,
+//   A[r,i] = sum_c q_rc k_ic exp(g_rc - g_ic),   i <= r in the same tile,
+// on CUDA cores, which is the evaluation that needs no bound on the decay
+// (the orkas.ai page, "Kimi K3 architecture", section "Eine Untergrenze,
+// die einen GPU-Codepfad beseitigte", describes the previous generation's
+// kernels keeping such a path for the diagonal).  q and k (exact in bf16)
+// and g (fp32) are staged as [token][channel] in [0, 64K) of shared memory,
+// which is free once M1 is done; one thread per position pair walks the
+// channels starting at a thread-dependent offset so a warp's loads fall in
+// distinct banks.  res[0..1023] receives A_qk and res[1024..2047] A_kk, as
+// [tile][r % 16][i % 16].  Called by all 128 threads of the CTA.
+__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
+                                                     float* res) {
+  uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
+  uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
+  float* sg = reinterpret_cast<float*>(sbp + 32768);
+  const int c = tid;
+#pragma unroll 1
+  for (int t0 = 0; t0 < CH; t0 += 16) {
+    float qv[16], kv[16], gv[16];
+    tmem_ld16(tl + TA_Q + t0, qv);
+    tmem_ld16(tl + TA_K + t0, kv);
+    tmem_ld16(tl + TA_G + t0, gv);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      sq[(t0 + j) * DP + c] = __bfloat16_as_ushort(__float2bfloat16_rn(qv[j]));
+      sk[(t0 + j) * DP + c] = __bfloat16_as_ushort(__float2bfloat16_rn(kv[j]));
+      sg[(t0 + j) * DP + c] = gv[j];
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int pidx = tid; pidx < 4 * 136; pidx += 128) {
+    const int a = pidx / 136, idx = pidx - 136 * a;
+    int rr = 0;
+    while ((rr + 1) * (rr + 2) / 2 <= idx) ++rr;
+    const int ii = idx - rr * (rr + 1) / 2;
+    const int r = 16 * a + rr, i = 16 * a + ii;
+    float aq = 0.f, ak = 0.f;
+#pragma unroll 4
+    for (int cc = 0; cc < DP; ++cc) {
+      const int ch = (cc + tid) & (DP - 1);
+      const float e = ex2((sg[r * DP + ch] - sg[i * DP + ch]) * LOG2E);
+      const float ki = bf2f(sk[i * DP + ch]) * e;
+      aq = fmaf(bf2f(sq[r * DP + ch]), ki, aq);
+      ak = fmaf(bf2f(sk[r * DP + ch]), ki, ak);
+    }
+    res[(16 * a + rr) * 16 + ii] = aq;
+    res[1024 + (16 * a + rr) * 16 + ii] = ak;
+  }
+  __syncthreads();
+}
+
 struct IntraParams {
   const __nv_bfloat16* beta;
   uint8_t* records;
@@ -304,7 +362,7 @@ struct IntraParams {
   int check_decay;
 };
 
-template <int DIN>
+template <int DIN, bool PAIRS>
 __global__ void __launch_bounds__(128, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
@@ -484,6 +542,10 @@ __global__ void __launch_bounds__(128, 2)
     ok = wait_all(bar_mma, mma_phase);
   }
 
+  // per-pair diagonal tiles (ablation only), kept in the (k e^g)^T slot
+  float* s_pair = reinterpret_cast<float*>(sbp + A_KT);
+  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, s_pair);
+
   float* akk = reinterpret_cast<float*>(sbp + A_AKK);
   float* ti = reinterpret_cast<float*>(sbp + A_TI);
   const OperandLayout AQ = kmajor(sb + A_STG + REC_AQ, 0);
@@ -497,6 +559,13 @@ __global__ void __launch_bounds__(128, 2)
     {
       float a[64];
       tmem_ld64(tl + TA_A, a);
+      if (PAIRS) {  // this row's diagonal tile from the per-pair path
+        const int m = tid < CH ? tid : tid - CH;
+        const float* row = s_pair + (tid < CH ? 0 : 1024) + (m >> 4) * 256 + (m & 15) * 16;
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+          if ((i >> 4) == (m >> 4) && (i & 15) <= (m & 15)) a[i] = row[i & 15];
+      }
       if (warp < 2) {
         const int r = tid;
 #pragma unroll
@@ -513,6 +582,7 @@ __global__ void __launch_bounds__(128, 2)
         for (int i = 0; i < CH; ++i) akk[i * CH + r] = (i < r) ? br * a[i] : 0.f;
       }
     }
+    if (PAIRS) __syncthreads();  // s_pair is overwritten by (k e^g)^T below
     // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -726,7 +796,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       tc_fence_after_sync();
       const int valid = min(CH, len - CH * j);
       float o[64];
-      tmem_ld64(tl + TB_O + 64 * ob, o);
+      tmem_ld64(tl + TB_D + 128 * ob + 64, o);  // holds -O^T
       tc_fence_before_sync();
       mbar_arrive(&o_empty[ob]);  // the TMEM tile may be overwritten now
       if (v < DIN) {
@@ -734,7 +804,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
                     (size_t)h * DIN + v;
 #pragma unroll
         for (int r = 0; r < CH; ++r)
-          if (r < valid) store_out(out + (size_t)r * H * DIN, p.scale * o[r]);
+          if (r < valid) store_out(out + (size_t)r * H * DIN, -p.scale * o[r]);
       }
     }
   } else {
@@ -780,40 +850,49 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     }
     tmem_st_wait();
 
-    constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
-    constexpr uint32_t ID_U = make_idesc(128, 64, false, true, true, true);     // fp16, -A
-    constexpr uint32_t ID_O1 = make_idesc(128, 64, false, true, false, true);   // fp16
-    constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, false, true);  // fp16
-    constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
+    constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                  // bf16
+    constexpr uint32_t ID_D = make_idesc(128, 128, false, true, true, true);     // fp16, -A
+    constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, true, true);    // fp16, -A
+    constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);   // fp16
     uint32_t mma_phase = 0;
 
+    // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is issued
+    // as soon as record j lands, ahead of the chain's own products.
+    auto issue_m3 = [&](int j) {
+      const int b = j & 1;
+      const uint32_t rb = sb + (b ? B_REC1 : B_REC0), vb = sb + (b ? B_V1 : B_V0);
+      const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
+      const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
+#pragma unroll
+      for (int k0 = 0; k0 < CH; k0 += 16)
+        umma_bf16(tmem + TB_UT + 64 * b, desc_adv(dva, k0, true), desc_adv(dtb, k0, false), ID_V,
+                  k0 > 0);
+    };
+    if (ok && nchunks > 0 && tid == 0) issue_m3(0);
+
     for (int j = 0; j < nchunks && ok; ++j) {
-      // invariant: record j is resident; ST = fp16(S_j); TMEM S = S_j (not yet decayed)
+      // invariant: record j is resident and its M3 issued; ST = fp16(S_j);
+      // TMEM S = S_j (not yet decayed)
       const int buf = j & 1, ob = j & 1;
       const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
-      const uint32_t vb = sb + (buf ? B_V1 : B_V0);
-      const uint32_t to = tmem + TB_O + 64 * ob;
+      const uint32_t td = tmem + TB_D + 128 * ob;
       operands_ready();
       if (tid == 0) {
         if (j >= 2 && !mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1)) {
           *s_abort = 1;
           set_status(6);
         }
-        const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
-        const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
+        // M4 and the first half of M5 as one N = 128 product: W and q e^g
+        // are adjacent MN-major operands (the second 64-row block of N sits
+        // one leading-byte offset, 16 KB, after the first), so
+        //   D = -S^T [W; q e^g]^T = [-S^T W^T | -S^T (q e^g)^T]
+        // reads the S^T operand from shared memory once for both.
         const uint64_t dst = layout_desc(ST, 0, 0);
-        const uint64_t dwt = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
-        const uint64_t dqt = layout_desc(mnmajor(rb + REC_QT, 16384), 0, 0);
+        const uint64_t dwq = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
         tc_fence_after_sync();
 #pragma unroll
-        for (int k0 = 0; k0 < CH; k0 += 16)
-          umma_bf16(tmem + TB_U, desc_adv(dva, k0, true), desc_adv(dtb, k0, false), ID_V, k0 > 0);
-#pragma unroll
-        for (int k0 = 0; k0 < DP; k0 += 16) {
-          const uint64_t a = desc_adv(dst, k0, false, 16384);
-          umma_bf16(tmem + TB_U, a, desc_adv(dwt, k0, true), ID_U, 1);
-          umma_bf16(to, a, desc_adv(dqt, k0, true), ID_O1, k0 > 0);
-        }
+        for (int k0 = 0; k0 < DP; k0 += 16)
+          umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dwq, k0, true), ID_D, k0 > 0);
         umma_commit(bar_mma);
       }
       {  // decay the fp32 state by this chunk's e^{g_C} while the tensor core runs
@@ -831,11 +910,16 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       }
       if (!(ok = wait_chain(bar_mma, mma_phase))) break;
       mma_phase ^= 1u;
-      {  // U^T (fp16 operand): this thread's 32 tokens
-        float u[32];
-        tmem_ld16(tl + TB_U + 32 * half, *reinterpret_cast<float(*)[16]>(u));
-        tmem_ld16(tl + TB_U + 32 * half + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+      {  // U^T = U~^T - S^T W^T (fp16 operand): this thread's 32 tokens
+        float u[32], w[32];
+        const uint32_t tu = tl + TB_UT + 64 * buf + 32 * half, tw = tl + TB_D + 128 * ob + 32 * half;
+        tmem_ld16(tu, *reinterpret_cast<float(*)[16]>(u));
+        tmem_ld16(tu + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+        tmem_ld16(tw, *reinterpret_cast<float(*)[16]>(w));
+        tmem_ld16(tw + 16, *reinterpret_cast<float(*)[16]>(w + 16));
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] += w[i];
 #pragma unroll
         for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
       }
@@ -847,8 +931,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 #pragma unroll
         for (int k0 = 0; k0 < CH; k0 += 16) {
           const uint64_t a = desc_adv(dut, k0, false);
-          umma_bf16(to, a, desc_adv(daq, k0, false), ID_O2, 1);
-          umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);
+          umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);      // M6
+          umma_bf16(td + 64, a, desc_adv(daq, k0, false), ID_O2, 1);        // M5, second half
         }
         umma_commit(bar_mma);
         umma_commit(&o_full[ob]);
@@ -863,6 +947,11 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         }
         ++pending;
       }
+      if (more) {
+        if (!(ok = wait_chain(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
+        --pending;
+        if (tid == 0) issue_m3(j + 1);  // runs under the rebuild below
+      }
       {  // the fp16 state operand for the next chunk (and the final state)
         float sv[64];
         tmem_ld64(tl + TB_S + 64 * half, sv);
@@ -873,10 +962,6 @@ __global__ void __launch_bounds__(B_THREADS, 1)
           for (int c0 = 0; c0 < 64; ++c0)
             if (c_lo + c0 < DIN) p.s1[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
         }
-      }
-      if (more) {
-        if (!(ok = wait_chain(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
-        --pending;
       }
     }
     if (ok && nchunks == 0 && p.s1 && v < DIN) {  // no tokens: final state = initial state
@@ -943,18 +1028,20 @@ template <int DIN, typename OutT>
 cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tg, int* chunk_base,
                           uint8_t* records, int grid_chunks, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = set_smem(kda_intra_kernel<DIN>, A_SMEM);
-    if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory opt-in is a per-device function attribute; setting it
+  // on every call costs next to nothing
+  cudaError_t e = set_smem(kda_intra_kernel<DIN, false>, A_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true>, A_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
+  if (e != cudaSuccess) return e;
   IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
                  pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0};
-  kda_intra_kernel<DIN><<<dim3((unsigned)grid_chunks, (unsigned)pr.H), 128, A_SMEM, stream>>>(
-      tq, tk, tg, ip);
-  cudaError_t e = cudaGetLastError();
+  const dim3 grid((unsigned)grid_chunks, (unsigned)pr.H);
+  if (pr.diag_per_pair)
+    kda_intra_kernel<DIN, true><<<grid, 128, A_SMEM, stream>>>(tq, tk, tg, ip);
+  else
+    kda_intra_kernel<DIN, false><<<grid, 128, A_SMEM, stream>>>(tq, tk, tg, ip);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   StateParams sp{records, pr.initial_state, pr.final_state, pr.out, pr.cu_seqlens, chunk_base,
                  pr.T, pr.n_seq, pr.H, pr.scale};

@@ -30,6 +30,7 @@ struct ChunkProblem {
   int H, d;
   float scale;
   bool check_decay;
+  bool diag_per_pair;  // ablation: diagonal tiles per position pair on CUDA cores
 };
 
 // Device workspace the chunked prefill needs: per-(chunk, head) records

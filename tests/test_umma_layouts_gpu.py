@@ -51,6 +51,7 @@ CASES = [
     (128, 64, 128, 0, SW128, 0, 1, SW128, 0, 0, None),
     (128, 128, 64, 0, SW128, 0, 1, SW128, 1, 0, None),
     (128, 128, 64, 0, SW128, 0, 1, SW128, 0, 0, None),
+    (128, 128, 128, 0, SW128, 0, 1, SW128, 0, 0, None),  # two N blocks one LBO apart, K = 128
     (128, 16, 128, 0, SW128, 0, 1, SW128, 0, 16, 64),
     (128, 16, 128, 0, SW128, 0, 1, SW128, 0, 48, 64),
     (128, 32, 64, 0, SW128, 0, 1, SW128, 0, 32, 64),
