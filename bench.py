@@ -211,10 +211,6 @@ def time_call(fn, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
-# kernels one call launches: intra-chunk stage + state pass (+ the varlen plan)
-LAUNCHES_FIXED, LAUNCHES_VARLEN = 2, 3
-
-
 def extra_workloads(args, ws, dev, stream, x64, ms64):
     """The other prefill shapes, timed the same way (inputs resident, larger
     than L2), plus the per-pair diagonal ablation on the T = 65536 problem."""
@@ -273,19 +269,25 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
 
 
 def run_profile_case(local):
-    """Small, fixed case for ncu captures (a few GB on the device at most)."""
+    """Small, fixed case for ncu captures (a few GB on the device at most):
+    two prefills of B=1 T=32768 H=32 (long enough for the overlapped,
+    segmented schedule), two of the 8k workload (plain two-stage schedule)
+    and three decode steps."""
     from linear_attention_recurrence_fwd_gb300 import binding
     from linear_attention_recurrence_fwd_gb300 import inputs as gen
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = gen.WORKLOADS["prefill_8k"]
-    x = gen.workload_inputs(w, device=dev)
-    a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
-    out = torch.empty(x["v"].shape, dtype=torch.float32, device=dev)
-    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
-    for _ in range(3):
-        binding.kda_chunk_fwd(*a, x["initial_state"], out=out, final_state=fin)
+    for name, T in (("prefill_64k", 32768), ("prefill_8k", None)):
+        w = gen.WORKLOADS[name]
+        x = gen.workload_inputs(w, device=dev, T=T)
+        a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+        out = torch.empty(x["v"].shape, dtype=torch.float32, device=dev)
+        fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            binding.kda_chunk_fwd(*a, x["initial_state"], out=out, final_state=fin)
+        torch.cuda.synchronize()
+        del x, a, out, fin
     wd = gen.WORKLOADS["decode"]
     xd = gen.make_inputs(wd.B, 1, wd.H, 128, 128, wd.seed, init_std=wd.init_std, device=dev)
     d = [xd[k][:, 0].contiguous() for k in ("q", "k", "v", "log_alpha", "beta")]
@@ -293,6 +295,8 @@ def run_profile_case(local):
     for _ in range(3):
         binding.kda_decode_step(*d, xd["initial_state"], out=o)
     torch.cuda.synchronize()
+    if binding.kda_last_device_status() != 0:
+        raise SystemExit("device status error")
 
 
 def main():
@@ -308,8 +312,8 @@ def main():
     ap.add_argument("--skip-extra", action="store_true",
                     help="time only the headline prefill and the decode step")
     ap.add_argument("--case", choices=["bench", "ncu"], default="bench",
-                    help="ncu: only run the small profiling case (3 prefills at T=8192 "
-                         "H=32, then 3 decode steps) and exit")
+                    help="ncu: only run the small profiling case (2 prefills at T=32768 "
+                         "and 2 at T=8192, H=32, then 3 decode steps) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -420,6 +424,7 @@ def main():
         del out, fin
         extra = extra_workloads(args, ws, dev, stream, x, ms_max)
 
+    launches_per_call = binding.kda_chunk_fwd_launches(w.B, w.T, w.H)
     ms = reduce_max(ms_local, ws)
     dec_us = reduce_max(dec_us_local, ws)
     e2e_ms = reduce_max(e2e_ms_local, ws)
@@ -461,8 +466,9 @@ def main():
                    "steps": args.decode_steps, "workload": "256 seq x 32 heads x d128, fp32 out"},
         "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * LAUNCHES_FIXED,
-        "gpu_launches_note": f"{LAUNCHES_FIXED} per prefill call (intra-chunk stage, state pass)",
+        "gpu_launches": args.steps * launches_per_call,
+        "gpu_launches_note": f"{launches_per_call} per prefill call (intra-chunk stage and state "
+                             f"pass, per segment of the overlapped schedule)",
         "workloads": extra,
         "clocks": clocks,
         "cpu_baseline": cpu,

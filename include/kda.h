@@ -84,7 +84,12 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
  *                     bytes, 16-byte aligned, owned by the caller; it holds
  *                     the per-(chunk, head) intermediate records (65 KiB
  *                     each) passed from the intra-chunk stage to the state
- *                     pass.  Too small or NULL -> KDA_ERR_WORKSPACE.
+ *                     pass, and the fp32 state handed between segments of
+ *                     the sequence.  Too small or NULL -> KDA_ERR_WORKSPACE.
+ * Long sequences run as segments of chunks: the intra-chunk stage of one
+ * segment overlaps the state pass of the previous one on two internal
+ * streams (created once per device), forked from and joined back to
+ * `stream` with events, so the call stays ordered on `stream`.
  * The chunked evaluation (64-token chunks of four 16-token tiles) follows
  * the blockwise computation the orkas.ai page describes in section "Eine
  * Untergrenze, die einen GPU-Codepfad beseitigte".  out must not alias any
@@ -99,8 +104,14 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
                            cudaStream_t stream);
 
 /* Bytes of device workspace kda_chunk_fwd needs for this shape:
- * B * ceil(T / 64) * H * 66560. */
+ * B * ceil(T / 64) * H * 66560 + B * H * 65536. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
+/* Kernel launches one kda_chunk_fwd call of this shape makes on the current
+ * device (the schedule depends on the device's SM count): 2 for the plain
+ * two-stage schedule, 2 per segment for the overlapped one.  -1 on a bad
+ * argument or a CUDA error.  A diagnostic for profiling and benchmarks. */
+KDA_API int kda_chunk_fwd_launches(int B, int T, int H);
 
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that are not allowed to
@@ -135,7 +146,9 @@ KDA_API kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const v
  *   v               : [T_total, H, d_v] bf16;   beta : [T_total, H] bf16
  *   cu_seqlens      : DEVICE int32 [N + 1], non-decreasing, cu[0] = 0,
  *                     cu[N] = T_total; sequence n owns tokens cu[n]..cu[n+1]-1
- *   max_seqlen      : an upper bound on the longest sequence (sizes the grid)
+ *   max_seqlen      : an upper bound on the longest sequence (sizes the work
+ *                     list; a longer sequence flags KDA_ERR_INVALID_ARG in
+ *                     the device status word)
  *   initial_state   : [N, H, d_k, d_v] fp32 or NULL;  final_state likewise
  *   out             : [T_total, H, d_v]
  *   workspace       : at least kda_varlen_fwd_workspace_size() bytes
@@ -154,7 +167,8 @@ KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             float scale, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
-/* (T_total / 64 + N) * H * 66560 plus 4 (N + 1) bytes rounded up to 1 KiB. */
+/* (T_total / 64 + N) * H * 66560 + N * H * 65536, plus 4 (N + 1) bytes
+ * rounded up to 1 KiB. */
 KDA_API size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v);
 
 /*

@@ -24,6 +24,7 @@ STATUS = {
 }
 
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
+           "kda_chunk_fwd_launches",
            "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
            "kda_last_device_status", "kda_version"]
@@ -63,6 +64,8 @@ def load(path: str = LIB_PATH):
         lib.kda_chunk_fwd_workspace_size.restype = _sz
         lib.kda_varlen_fwd_workspace_size.argtypes = [_i] * 5
         lib.kda_varlen_fwd_workspace_size.restype = _sz
+        lib.kda_chunk_fwd_launches.argtypes = [_i, _i, _i]
+        lib.kda_chunk_fwd_launches.restype = _i
         lib.kda_status_string.argtypes = [_i]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_last_device_status.argtypes = [_vp]
@@ -201,6 +204,11 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, scale=1.0, out=None,
                                _dtype_code(out.dtype), N, H, dk, dv, float(scale),
                                _stream(stream)), "kda_decode_step")
     return out
+
+
+def kda_chunk_fwd_launches(B, T, H):
+    """Kernel launches one kda_chunk_fwd call of this shape makes on the current device."""
+    return int(load().kda_chunk_fwd_launches(int(B), int(T), int(H)))
 
 
 def kda_last_device_status(stream=None) -> int:

@@ -27,6 +27,13 @@ bool ablate_diag_env() {
   return e && e[0] && e[0] != '0';
 }
 
+// The intra-chunk stage walks a work list of (sequence, chunk, head) items
+// indexed by int; sequences x chunks of the longest x heads must stay below this.
+constexpr long long kMaxItems = 1LL << 30;
+long long work_items(int n_seq, int max_len, int H) {
+  return (long long)n_seq * ((max_len + 63) / 64) * H;
+}
+
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 kda_status_t validate_prefill(const void* q, const void* k, const void* v, const void* la,
@@ -87,7 +94,7 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
                                      final_state, H, d_k, d_v, (long long)B * T > 0);
   if (st != KDA_OK) return st;
-  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
   if (B == 0) return KDA_OK;
   const size_t need = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v);
   if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -107,7 +114,7 @@ kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
   kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
                                      final_state, H, d_k, d_v, (long long)B * T > 0);
   if (st != KDA_OK) return st;
-  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
   if (B == 0) return KDA_OK;
   const long long records = (long long)B * ((T + 63) / 64) * H;
   if (records > (long long)kda::noalloc_max_records()) return KDA_ERR_WORKSPACE;
@@ -129,6 +136,7 @@ kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v, const v
   kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
                                      final_state, H, d_k, d_v, T_total > 0);
   if (st != KDA_OK) return st;
+  if (work_items(N, max_seqlen, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
   if (N == 0) return KDA_OK;
   const size_t need = kda_varlen_fwd_workspace_size(N, T_total, H, d_k, d_v);
   if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -154,6 +162,11 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
   if (N == 0) return KDA_OK;
   return from_cuda(kda::launch_decode_step(q, k, v, log_alpha, beta, state, out,
                                            out_dtype == KDA_F32, N, H, scale, stream));
+}
+
+int kda_chunk_fwd_launches(int B, int T, int H) {
+  if (B < 0 || T < 0 || H <= 0) return -1;
+  return kda::chunk_fwd_launches(false, B, T, H);
 }
 
 kda_status_t kda_last_device_status(cudaStream_t stream) {

@@ -54,6 +54,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kda_internal.h"
@@ -88,10 +89,14 @@ constexpr uint32_t A_KBH = 65536, A_KBL = 81920;          // M1 B operand     (M
 constexpr uint32_t A_STG = 0;                             // record image [0, 64K) (after M1)
 constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][64]  (after M1)
 constexpr uint32_t A_KT = 81920;                          // (k e^g)^T bf16      (after M1)
+constexpr uint32_t A_WST = 81920;                         // W record image      (after M2)
 constexpr uint32_t A_TI = 0;                              // T fp32 (in the W slot, before W)
 constexpr uint32_t A_DINV = 57344;                        // T_aa transposed, 4 KB (in the T diag(beta) slot, before it)
 constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
-constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
+constexpr uint32_t A_SLOT = A_MISC + 1024;                // one slot's shared memory
+constexpr uint32_t A_SMEM = 2 * A_SLOT + 1024;            // two slots + alignment slack
+constexpr int A_THREADS = 256;                            // two slots of 128 threads
+constexpr uint32_t A_SMEM_ONE = A_SLOT + 1024;            // one slot (one item per CTA)
 
 // ---- stage 2 shared memory
 constexpr uint32_t B_REC0 = 0, B_V0 = 66560, B_REC1 = 82944, B_V1 = 149504;
@@ -101,7 +106,8 @@ constexpr uint32_t B_MISC = 215040;
 constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
-constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
+constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0;  // within a slot
+constexpr uint32_t TA_SLOT_COLS = 256, TA_COLS = 512;
 // Stage 2: U~ (M3 result, two buffers), D = [-S^T W^T | -O^T] (two buffers of
 // 128 columns: the U correction and the output share one N = 128 product)
 // and the fp32 state S^T.
@@ -181,42 +187,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 
 __device__ __forceinline__ void set_status(int code) { atomicExch(&g_chunk_status, code); }
 
-// Chunk -> (sequence, first token, valid tokens).  Packed sequences use the
-// per-sequence chunk offsets (chunk_base[n] = chunks before sequence n).
-struct ChunkLoc {
-  int n, j, t0, valid, ok;
-};
-__device__ __forceinline__ ChunkLoc locate_chunk(int q, const int* cu, const int* base, int n_seq,
-                                                 int T) {
-  ChunkLoc L;
-  int len, seq0;
-  if (cu) {
-    if (q >= base[n_seq]) {
-      L.ok = 0;
-      return L;
-    }
-    int lo = 0, hi = n_seq;  // base[lo] <= q < base[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (base[mid] <= q) lo = mid; else hi = mid;
-    }
-    L.n = lo;
-    L.j = q - base[lo];
-    seq0 = cu[lo];
-    len = cu[lo + 1] - seq0;
-  } else {
-    const int nc = (T + CH - 1) / CH;
-    L.n = q / nc;
-    L.j = q % nc;
-    seq0 = L.n * T;
-    len = T;
-  }
-  L.t0 = seq0 + CH * L.j;
-  L.valid = min(CH, len - CH * L.j);
-  L.ok = 1;
-  return L;
-}
-
 // Version b of the M1 A operand: rows r >= 16 b of [Q^(b); K^(b)] with
 // Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r F[tile(r)][b] (same for K),
 // as bf16 hi/lo pairs.  Rows above 16 b are never read back.
@@ -246,6 +216,12 @@ __device__ __forceinline__ void build_version(const OperandLayout& XH, const Ope
   }
 }
 
+// Stage 1 runs two independent items per CTA ("slots", 128 threads each);
+// a slot synchronises on its own named barrier (1 or 2).
+__device__ __forceinline__ void slot_sync(int slot) {
+  asm volatile("bar.sync %0, 128;" ::"r"(slot + 1) : "memory");
+}
+
 // T (fp32 64x64) with 16-byte chunks XOR-swizzled by row.
 __device__ __forceinline__ int tix(int r, int c) {
   return r * CH + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
@@ -256,7 +232,7 @@ __device__ __forceinline__ int tix(int r, int c) {
 // = T_aa[rr][x]; P goes to the unused upper-triangle block (b, a) of ti.
 template <int S>
 __device__ __forceinline__ void solve_level(const float* akk, float* ti, const float* dinv,
-                                            int tid) {
+                                            int tid, int slot) {
   constexpr int kStrips = (4 - S) * 64;  // (block, row, 4-column quad)
 #pragma unroll
   for (int st = tid; st < kStrips; st += 128) {
@@ -278,7 +254,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
     *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) =
         make_float4(acc0, acc1, acc2, acc3);
   }
-  __syncthreads();
+  slot_sync(slot);
 #pragma unroll
   for (int st = tid; st < kStrips; st += 128) {
     const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
@@ -295,7 +271,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
     *reinterpret_cast<float4*>(ti + tix(16 * a + rr, 16 * b + 4 * q)) =
         make_float4(-acc0, -acc1, -acc2, -acc3);
   }
-  __syncthreads();
+  slot_sync(slot);
 }
 
 // Ablation of the dense diagonal tiles: the four 16x16 diagonal tiles of
@@ -309,8 +285,8 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
 // which is free once M1 is done; one thread per position pair walks the
 // channels starting at a thread-dependent offset so a warp's loads fall in
 // distinct banks.  res[0..1023] receives A_qk and res[1024..2047] A_kk, as
-// [tile][r % 16][i % 16].  Called by all 128 threads of the CTA.
-__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
+// [tile][r % 16][i % 16].  Called by all 128 threads of a slot.
+__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid, int slot,
                                                      float* res) {
   uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
   uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
@@ -330,7 +306,7 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
       sg[(t0 + j) * DP + c] = gv[j];
     }
   }
-  __syncthreads();
+  slot_sync(slot);
 #pragma unroll 1
   for (int pidx = tid; pidx < 4 * 136; pidx += 128) {
     const int a = pidx / 136, idx = pidx - 136 * a;
@@ -350,9 +326,11 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
     res[(16 * a + rr) * 16 + ii] = aq;
     res[1024 + (16 * a + rr) * 16 + ii] = ak;
   }
-  __syncthreads();
+  slot_sync(slot);
 }
 
+// Stage 1 work list: item w = ((n * seg_len) + (j - j_lo)) * H + h covers
+// chunk j of sequence n, head h, for chunks j in [j_lo, j_lo + seg_len).
 struct IntraParams {
   const __nv_bfloat16* beta;
   uint8_t* records;
@@ -360,41 +338,116 @@ struct IntraParams {
   const int* chunk_base;
   int T, n_seq, H;
   int check_decay;
+  int j_lo, seg_len, n_items;
 };
 
-template <int DIN, bool PAIRS>
-__global__ void __launch_bounds__(128, 2)
+template <int DIN, bool PAIRS, bool PERSIST>
+__global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
-  const ChunkLoc loc = locate_chunk(blockIdx.x, p.cu, p.chunk_base, p.n_seq, p.T);
-  if (!loc.ok) return;  // packed grids are sized for the worst case
+  // PERSIST: each CTA holds one SM (two slots' shared memory) and its two
+  // slots walk the work list independently, so a launch that leaves some SMs
+  // out leaves them entirely free.  Otherwise one CTA (one slot) per item,
+  // two CTAs per SM.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.y, H = p.H, valid = loc.valid;
+  constexpr uint32_t kCols = PERSIST ? TA_COLS : TA_SLOT_COLS;
+  const int slot = PERSIST ? threadIdx.x >> 7 : 0;
+  const int tid = threadIdx.x & 127, warp = tid >> 5;  // within the slot
+  const int H = p.H;
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;
+  const uint32_t sb0 = (raw + 1023u) & ~1023u;
+  const uint32_t sb = sb0 + (uint32_t)slot * A_SLOT;
   uint8_t* sbp = smem_raw + (sb - raw);
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sbp + A_MISC);
   uint64_t* bar_mma = bar_tma + 1;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + A_MISC + 16);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem_raw + (sb0 - raw) + A_MISC + 16);
   int* s_abort = reinterpret_cast<int*>(sbp + A_MISC + 20);
   float* s_beta = reinterpret_cast<float*>(sbp + A_MISC + 64);    // [64]
   float* s_gamma = reinterpret_cast<float*>(sbp + A_MISC + 512);  // [128], 16-byte aligned
-  uint8_t* rec = p.records + ((size_t)blockIdx.x * H + h) * REC_BYTES;
 
   if (tid == 0) {
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     mbar_fence_init();
     *s_abort = 0;
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(tmem_base_s, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_all = *tmem_base_s;
+  const uint32_t tmem = tmem_all + TA_SLOT_COLS * (uint32_t)slot;
+  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+  uint32_t tma_phase = 0, mma_phase = 0;
+  bool ok = true;
+
+  auto wait_all = [&](uint64_t* bar, uint32_t& phase) -> bool {
+    if (!mbar_wait(bar, phase)) {
+      *s_abort = 1;
+      set_status(6);
+    }
+    phase ^= 1u;
+    slot_sync(slot);
+    tc_fence_after_sync();
+    return *s_abort == 0;
+  };
+  auto operands_ready = [&]() {
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    slot_sync(slot);
+    tc_fence_after_sync();
+  };
+
+  // item w -> head, first token, valid tokens and record index (valid <= 0:
+  // past the end of a packed sequence)
+  struct Item {
+    int h, t0, valid, qrec;
+  };
+  auto item_of = [&](int w) {
+    Item it;
+    it.h = w % H;
+    const int item_r = w / H;
+    const int n = item_r / p.seg_len, jc = p.j_lo + item_r % p.seg_len;
+    int seq0, len;
+    if (p.cu) {
+      seq0 = p.cu[n];
+      len = p.cu[n + 1] - seq0;
+      it.qrec = p.chunk_base[n] + jc;
+    } else {
+      seq0 = n * p.T;
+      len = p.T;
+      it.qrec = n * ((p.T + CH - 1) / CH) + jc;
+    }
+    it.t0 = seq0 + CH * jc;
+    it.valid = min(CH, len - CH * jc);
+    return it;
+  };
+  const int stride = PERSIST ? 2 * (int)gridDim.x : (int)gridDim.x;
+  for (int w = PERSIST ? 2 * (int)blockIdx.x + slot : (int)blockIdx.x; ok && w < p.n_items;
+       w += stride) {
+  const Item cur = item_of(w);
+  if (cur.valid <= 0) continue;
+  const int h = cur.h, t0 = cur.t0, valid = cur.valid, qrec = cur.qrec;
+  uint8_t* rec = p.records + ((size_t)qrec * H + h) * REC_BYTES;
+
+  if (tid == 0) {
+    // The previous item's stores: all but its last group (W, T diag(beta),
+    // e^{g_C}) are done reading shared memory, and that last group reads
+    // only space this item's loads and L, I do not touch.
+    bulk_wait_reads_but_last();
     mbar_arrive_expect_tx(bar_tma, 3u * (DIN / 64) * 8192u);
 #pragma unroll
     for (int b = 0; b < DIN / 64; ++b) {
-      tma_load_3d(sbp + A_RQ + b * 8192, &tm_q, bar_tma, b * 64, h, loc.t0);
-      tma_load_3d(sbp + A_RK + b * 8192, &tm_k, bar_tma, b * 64, h, loc.t0);
-      tma_load_3d(sbp + A_RG + b * 8192, &tm_g, bar_tma, b * 64, h, loc.t0);
+      tma_load_3d(sbp + A_RQ + b * 8192, &tm_q, bar_tma, b * 64, h, t0);
+      tma_load_3d(sbp + A_RK + b * 8192, &tm_k, bar_tma, b * 64, h, t0);
+      tma_load_3d(sbp + A_RG + b * 8192, &tm_g, bar_tma, b * 64, h, t0);
     }
   }
+  const float beta_t = tid < valid ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+  slot_sync(slot);
   if (DIN == 64) {  // upper channel half of the raw tiles stays zero
     for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
       st_shared_v4(sb + A_RQ + 8192 + off, 0, 0, 0, 0);
@@ -402,8 +455,6 @@ __global__ void __launch_bounds__(128, 2)
       st_shared_v4(sb + A_RG + 8192 + off, 0, 0, 0, 0);
     }
   }
-  const float beta_t =
-      tid < valid ? __bfloat162float(p.beta[(size_t)(loc.t0 + tid) * H + h]) : 0.f;
   // L[r][i] = (i <= r), I[r][i] = (i == r), both restricted to valid tokens i
   const OperandLayout LM = kmajor(sb + A_LM, 0), IM = kmajor(sb + A_IM, 0);
   {
@@ -422,37 +473,12 @@ __global__ void __launch_bounds__(128, 2)
     }
   }
   if (tid < CH) s_beta[tid] = beta_t;
-  if (warp == 0) {
-    tmem_alloc(tmem_base_s, TA_COLS);
-    tmem_relinquish();
-  }
   fence_proxy_async_smem();
   tc_fence_before_sync();
-  __syncthreads();
+  slot_sync(slot);
   tc_fence_after_sync();
-  const uint32_t tmem = *tmem_base_s;
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-  uint32_t mma_phase = 0;
 
-  auto wait_all = [&](uint64_t* bar, uint32_t& phase) -> bool {
-    if (!mbar_wait(bar, phase)) {
-      *s_abort = 1;
-      set_status(6);
-    }
-    phase ^= 1u;
-    __syncthreads();
-    tc_fence_after_sync();
-    return *s_abort == 0;
-  };
-  auto operands_ready = [&]() {
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-  };
-
-  uint32_t tma_phase = 0;
-  bool ok = wait_all(bar_tma, tma_phase);
+  ok = wait_all(bar_tma, tma_phase);
   const int c = tid;  // key channel owned in the elementwise stages
   if (ok && p.check_decay) {
     bool bad = false;
@@ -502,6 +528,10 @@ __global__ void __launch_bounds__(128, 2)
   const OperandLayout XH = mnmajor(sb + A_XH, 16384), XL = mnmajor(sb + A_XL, 16384);
   const OperandLayout KBH = mnmajor(sb + A_KBH, 16384), KBL = mnmajor(sb + A_KBL, 16384);
   constexpr uint32_t ID_M1 = make_idesc(128, 16, true, true);
+  // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
+  // M1 operands below overwrite
+  if (tid == 0) bulk_wait_reads();
+  slot_sync(slot);
   if (ok) {
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -544,7 +574,7 @@ __global__ void __launch_bounds__(128, 2)
 
   // per-pair diagonal tiles (ablation only), kept in the (k e^g)^T slot
   float* s_pair = reinterpret_cast<float*>(sbp + A_KT);
-  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, s_pair);
+  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, slot, s_pair);
 
   float* akk = reinterpret_cast<float*>(sbp + A_AKK);
   float* ti = reinterpret_cast<float*>(sbp + A_TI);
@@ -553,7 +583,7 @@ __global__ void __launch_bounds__(128, 2)
   const OperandLayout KBAR = kmajor(sb + A_STG + REC_KBAR, 0);
   const OperandLayout KT = kmajor(sb + A_KT, 0);
   const OperandLayout TB = kmajor(sb + A_STG + REC_TB, 0);
-  const OperandLayout WT = mnmajor(sb + A_STG + REC_WT, 16384);
+  const OperandLayout WT = mnmajor(sb + A_WST, 16384);
   if (ok) {
     // ---- A_qk (fp16 record image) and beta-scaled strictly-lower A_kk (fp32)
     {
@@ -582,7 +612,7 @@ __global__ void __launch_bounds__(128, 2)
         for (int i = 0; i < CH; ++i) akk[i * CH + r] = (i < r) ? br * a[i] : 0.f;
       }
     }
-    if (PAIRS) __syncthreads();  // s_pair is overwritten by (k e^g)^T below
+    if (PAIRS) slot_sync(slot);  // s_pair is overwritten by (k e^g)^T below
     // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -609,7 +639,7 @@ __global__ void __launch_bounds__(128, 2)
     }
     s_gamma[c] = GE[3];
     fence_proxy_async_smem();
-    __syncthreads();
+    slot_sync(slot);
     if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
       bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
       bulk_commit();
@@ -637,12 +667,12 @@ __global__ void __launch_bounds__(128, 2)
 #pragma unroll
       for (int q = 0; q < 4; ++q) drow[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
-    __syncthreads();
+    slot_sync(slot);
     // off-diagonal blocks by distance s = a - b: P = sum_{m=b}^{a-1} L_am T_mb,
     // then T_ab = -T_aa P.  A thread owns a strip of 4 columns of one row.
-    solve_level<1>(akk, ti, dinv, tid);
-    solve_level<2>(akk, ti, dinv, tid);
-    solve_level<3>(akk, ti, dinv, tid);
+    solve_level<1>(akk, ti, dinv, tid, slot);
+    solve_level<2>(akk, ti, dinv, tid, slot);
+    solve_level<3>(akk, ti, dinv, tid, slot);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
       const int r = tid >> 1, i_lo = (tid & 1) * 32;
@@ -678,38 +708,47 @@ __global__ void __launch_bounds__(128, 2)
 #pragma unroll
     for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(WT, r0, c), w + r0);
     fence_proxy_async_smem();
-    __syncthreads();
+    slot_sync(slot);
     if (tid == 0) {
-      bulk_s2g(rec + REC_WT, sb + A_STG + REC_WT, REC_QT - REC_WT);
+      bulk_s2g(rec + REC_WT, sb + A_WST, REC_QT - REC_WT);
       bulk_s2g(rec + REC_TB, sb + A_STG + REC_TB, REC_G - REC_TB);
       bulk_s2g(rec + REC_G, smem_u32(s_gamma), 512);
       bulk_commit();
     }
   }
+  }  // items
   if (tid == 0) bulk_wait_all();
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, TA_COLS);
+  if (threadIdx.x < 32) tmem_dealloc(tmem_all, kCols);
 }
 
+// Stage 2 covers chunks [j_lo, j_hi) of every sequence.  The state entering
+// chunk j_lo is s0 when j_lo == 0, else the carried state; the state after a
+// sequence's last chunk goes to s1, else (the range ends earlier) to carry.
 struct StateParams {
   const uint8_t* records;
   const float* s0;
   float* s1;
+  float* carry;  // [n_seq][H][128][128] fp32, or null for a single range
   void* out;
   const int* cu;
   const int* chunk_base;
   int T, n_seq, H;
+  int j_lo, j_hi;
   float scale;
 };
 
-// Stage 2 warp roles: warps 0-7 run the serial chain (two per TMEM lane
-// quadrant, splitting columns); warps 8-11 drain finished output tiles from
-// TMEM to global memory, double-buffered, off the chain.
+// Stage 2 warp roles: warps 0-7 run the elementwise part of the serial
+// chain (two per TMEM lane quadrant, splitting columns); warps 8-11 drain
+// finished output tiles from TMEM to global memory, double-buffered; warp 12
+// (one lane) issues every MMA and every load.  Issuing is kept off the chain
+// warps because an issuing thread stalls while the tensor core's queue is
+// full.  Hand-offs are mbarriers (bounded waits), never named barriers, so
+// a timeout anywhere unwinds every role.
 constexpr int B_CHAIN = 256;
-constexpr int B_THREADS = 384;
-
-__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+constexpr int B_OUTPUT = 128;
+constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
 
 template <int DIN, typename OutT>
 __global__ void __launch_bounds__(B_THREADS, 1)
@@ -723,11 +762,14 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sbp = smem_raw + (sb - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sbp + B_MISC);  // [2] record + v tile landed
-  uint64_t* bar_mma = full + 2;                                // chain MMAs done
-  uint64_t* o_full = full + 3;                                 // [2] output tile ready
-  uint64_t* o_empty = full + 5;                                // [2] output tile drained
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 64);
-  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 68);
+  uint64_t* mma_a = full + 2;     // D = -S^T [W; q e^g]^T done
+  uint64_t* mma_b = full + 3;     // S update and the rest of O done
+  uint64_t* o_full = full + 4;    // [2] output tile ready
+  uint64_t* o_empty = full + 6;   // [2] output tile drained
+  uint64_t* st_ready = full + 8;  // chain -> issuer: S^T operand written
+  uint64_t* ut_ready = full + 9;  // chain -> issuer: U^T operand written, state decayed
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 96);
+  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 100);
 
   int tok0, len, base;
   if (p.cu) {
@@ -739,18 +781,28 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     len = p.T;
     base = n * ((p.T + CH - 1) / CH);
   }
-  const int nchunks = len > 0 ? (len + CH - 1) / CH : 0;
+  const int nch_seq = len > 0 ? (len + CH - 1) / CH : 0;
+  const int jb = p.j_lo, nchunks = max(0, min(p.j_hi, nch_seq) - jb);  // j below is jb + local
+  const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+  if (nchunks == 0) {  // nothing in this range; a sequence with no tokens keeps its state
+    if (jb == 0 && nch_seq == 0 && p.s1)
+      for (int i = threadIdx.x; i < DIN * DIN; i += blockDim.x)
+        p.s1[sbase + i] = p.s0 ? p.s0[sbase + i] : 0.f;
+    return;
+  }
+  const float* s_in = jb == 0 ? p.s0 : p.carry;
+  float* s_out = jb + nchunks == nch_seq ? p.s1 : p.carry;
   constexpr uint32_t kVBytes = (DIN / 64) * 8192u;
 
   auto issue_loads = [&](int j, int buf) {
-    const uint8_t* rec = p.records + ((size_t)(base + j) * H + h) * REC_BYTES;
+    const uint8_t* rec = p.records + ((size_t)(base + jb + j) * H + h) * REC_BYTES;
     uint8_t* dst = sbp + (buf ? B_REC1 : B_REC0);
     uint8_t* vdst = sbp + (buf ? B_V1 : B_V0);
     mbar_arrive_expect_tx(&full[buf], REC_LOAD + kVBytes);
     bulk_g2s(dst, rec, REC_LOAD, &full[buf]);
 #pragma unroll
     for (int b = 0; b < DIN / 64; ++b)
-      tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * j);
+      tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * (jb + j));
   };
   auto gamma_of = [&](int buf) {
     return reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
@@ -759,11 +811,14 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(mma_a, 1);
+    mbar_init(mma_b, 1);
     mbar_init(&o_full[0], 1);
     mbar_init(&o_full[1], 1);
-    mbar_init(&o_empty[0], B_THREADS - B_CHAIN);
-    mbar_init(&o_empty[1], B_THREADS - B_CHAIN);
+    mbar_init(&o_empty[0], B_OUTPUT);
+    mbar_init(&o_empty[1], B_OUTPUT);
+    mbar_init(st_ready, B_CHAIN);
+    mbar_init(ut_ready, B_CHAIN);
     mbar_fence_init();
     *s_abort = 0;
     if (nchunks > 0) issue_loads(0, 0);
@@ -779,28 +834,114 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     tmem_alloc(tmem_base_s, TB_COLS);
     tmem_relinquish();
   }
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_s;
   const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
+  const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
+  auto fail = [&]() {
+    *s_abort = 1;
+    set_status(6);
+  };
 
-  if (tid >= B_CHAIN) {
+  if (warp == B_THREADS / 32 - 1) {
+    // ---------------- issuer: one lane issues every MMA and every load
+    if ((tid & 31) == 0 && nchunks > 0) {
+      constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
+      constexpr uint32_t ID_D = make_idesc(128, 128, false, true, true, true);    // fp16, -A
+      constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, true, true);   // fp16, -A
+      constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
+      // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is
+      // issued as soon as record j lands, ahead of the chain's own products.
+      auto issue_m3 = [&](int j) {
+        const int b = j & 1;
+        const uint32_t rb = sb + (b ? B_REC1 : B_REC0), vb = sb + (b ? B_V1 : B_V0);
+        const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
+        const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
+#pragma unroll
+        for (int k0 = 0; k0 < CH; k0 += 16)
+          umma_bf16(tmem + TB_UT + 64 * b, desc_adv(dva, k0, true), desc_adv(dtb, k0, false),
+                    ID_V, k0 > 0);
+      };
+      int issued = min(nchunks, 2), landed = 0;  // record loads issued / seen complete
+      bool ok = mbar_wait(&full[0], 0);
+      if (ok) {
+        landed = 1;
+        tc_fence_after_sync();
+        issue_m3(0);
+      }
+      for (int j = 0; j < nchunks && ok; ++j) {
+        const int buf = j & 1, ob = j & 1;
+        const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
+        const uint32_t td = tmem + TB_D + 128 * ob;
+        if (!(ok = mbar_wait(st_ready, j & 1))) break;
+        if (j >= 2 && !(ok = mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1))) break;
+        tc_fence_after_sync();
+        {  // M4 and the first half of M5 as one N = 128 product: W and q e^g are
+           // adjacent MN-major operands (the second 64-row block of N sits one
+           // leading-byte offset, 16 KB, after the first), so
+           //   D = -S^T [W; q e^g]^T = [-S^T W^T | -S^T (q e^g)^T]
+           // reads the S^T operand from shared memory once for both.
+          const uint64_t dst = layout_desc(ST, 0, 0);
+          const uint64_t dwq = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
+#pragma unroll
+          for (int k0 = 0; k0 < DP; k0 += 16)
+            umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dwq, k0, true), ID_D, k0 > 0);
+          umma_commit(mma_a);
+        }
+        if (!(ok = mbar_wait(ut_ready, j & 1))) break;
+        tc_fence_after_sync();
+        {
+          const uint64_t dut = layout_desc(UT, 0, 0);
+          const uint64_t daq = layout_desc(kmajor(rb + REC_AQ, 0), 0, 0);
+          const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
+#pragma unroll
+          for (int k0 = 0; k0 < CH; k0 += 16) {
+            const uint64_t a = desc_adv(dut, k0, false);
+            umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);  // M6
+            umma_bf16(td + 64, a, desc_adv(daq, k0, false), ID_O2, 1);    // M5, second half
+          }
+          umma_commit(mma_b);
+          umma_commit(&o_full[ob]);
+        }
+        if (j + 2 < nchunks) {  // buffer buf is consumed once every product of chunk j is done
+          if (!(ok = mbar_wait(mma_b, j & 1))) break;
+          fence_proxy_async_smem();
+          issue_loads(j + 2, buf);
+          ++issued;
+        }
+        if (j + 1 < nchunks) {
+          if (!(ok = mbar_wait(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
+          ++landed;
+          tc_fence_after_sync();
+          issue_m3(j + 1);
+        }
+      }
+      if (!ok) {
+        fail();
+        // let copies already issued land before the CTA's memory goes away
+        for (int r = landed; r < issued; ++r) mbar_wait(&full[r & 1], (r >> 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp >= B_CHAIN / 32) {
     // ---------------- output warps: thread = value channel v, all 64 tokens
     for (int j = 0; j < nchunks; ++j) {
       const int ob = j & 1;
       if (!mbar_wait(&o_full[ob], (j >> 1) & 1)) {
-        set_status(6);
+        fail();
         break;
       }
       tc_fence_after_sync();
-      const int valid = min(CH, len - CH * j);
+      const int valid = min(CH, len - CH * (jb + j));
       float o[64];
       tmem_ld64(tl + TB_D + 128 * ob + 64, o);  // holds -O^T
       tc_fence_before_sync();
       mbar_arrive(&o_empty[ob]);  // the TMEM tile may be overwritten now
       if (v < DIN) {
-        OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * j) * H * DIN +
+        OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * (jb + j)) * H * DIN +
                     (size_t)h * DIN + v;
 #pragma unroll
         for (int r = 0; r < CH; ++r)
@@ -808,33 +949,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       }
     }
   } else {
-    // ---------------- chain warps
-    const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
-    const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
-    auto wait_chain = [&](uint64_t* bar, uint32_t phase) -> bool {
-      if (!mbar_wait(bar, phase)) {
-        *s_abort = 1;
-        set_status(6);
-      }
-      chain_sync();
-      tc_fence_after_sync();
-      return *s_abort == 0;
-    };
-    auto operands_ready = [&]() {
-      fence_proxy_async_smem();
-      tc_fence_before_sync();
-      chain_sync();
-      tc_fence_after_sync();
-    };
-
-    bool ok = true;
-    int pending = min(nchunks, 2);  // record loads in flight
-    if (nchunks > 0) {
-      ok = wait_chain(&full[0], 0);
-      if (ok) --pending;
-    }
+    // ---------------- chain warps: decay, U^T and S^T operands, final state
     // initial state: thread (v, half) holds S^T[v][64 half .. 64 half + 63]
-    const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
     const int c_lo = 64 * half;
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
@@ -842,59 +958,21 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         const int c = c_lo + c0 + jj;
-        s0[jj] = (p.s0 && c < DIN && v < DIN) ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
+        s0[jj] = (s_in && c < DIN && v < DIN) ? s_in[sbase + (size_t)c * DIN + v] : 0.f;
       }
       tmem_st16(tl + TB_S + c_lo + c0, s0);
       st8h(layout_addr(ST, v, c_lo + c0), s0);
       st8h(layout_addr(ST, v, c_lo + c0 + 8), s0 + 8);
     }
     tmem_st_wait();
-
-    constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                  // bf16
-    constexpr uint32_t ID_D = make_idesc(128, 128, false, true, true, true);     // fp16, -A
-    constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, true, true);    // fp16, -A
-    constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);   // fp16
-    uint32_t mma_phase = 0;
-
-    // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is issued
-    // as soon as record j lands, ahead of the chain's own products.
-    auto issue_m3 = [&](int j) {
-      const int b = j & 1;
-      const uint32_t rb = sb + (b ? B_REC1 : B_REC0), vb = sb + (b ? B_V1 : B_V0);
-      const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
-      const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
-#pragma unroll
-      for (int k0 = 0; k0 < CH; k0 += 16)
-        umma_bf16(tmem + TB_UT + 64 * b, desc_adv(dva, k0, true), desc_adv(dtb, k0, false), ID_V,
-                  k0 > 0);
-    };
-    if (ok && nchunks > 0 && tid == 0) issue_m3(0);
-
-    for (int j = 0; j < nchunks && ok; ++j) {
-      // invariant: record j is resident and its M3 issued; ST = fp16(S_j);
-      // TMEM S = S_j (not yet decayed)
+    bool ok = true;
+    for (int j = 0; j < nchunks; ++j) {
+      // invariant: ST = fp16(S_j) written by this thread; TMEM S = S_j
       const int buf = j & 1, ob = j & 1;
-      const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
-      const uint32_t td = tmem + TB_D + 128 * ob;
-      operands_ready();
-      if (tid == 0) {
-        if (j >= 2 && !mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1)) {
-          *s_abort = 1;
-          set_status(6);
-        }
-        // M4 and the first half of M5 as one N = 128 product: W and q e^g
-        // are adjacent MN-major operands (the second 64-row block of N sits
-        // one leading-byte offset, 16 KB, after the first), so
-        //   D = -S^T [W; q e^g]^T = [-S^T W^T | -S^T (q e^g)^T]
-        // reads the S^T operand from shared memory once for both.
-        const uint64_t dst = layout_desc(ST, 0, 0);
-        const uint64_t dwq = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
-        tc_fence_after_sync();
-#pragma unroll
-        for (int k0 = 0; k0 < DP; k0 += 16)
-          umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dwq, k0, true), ID_D, k0 > 0);
-        umma_commit(bar_mma);
-      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(st_ready);
+      if (!(ok = mbar_wait(&full[buf], (j >> 1) & 1))) break;
       {  // decay the fp32 state by this chunk's e^{g_C} while the tensor core runs
         const float* gam = gamma_of(buf);
         float sv[64];
@@ -908,8 +986,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         }
         tmem_st_wait();
       }
-      if (!(ok = wait_chain(bar_mma, mma_phase))) break;
-      mma_phase ^= 1u;
+      if (!(ok = mbar_wait(mma_a, j & 1))) break;
+      tc_fence_after_sync();
       {  // U^T = U~^T - S^T W^T (fp16 operand): this thread's 32 tokens
         float u[32], w[32];
         const uint32_t tu = tl + TB_UT + 64 * buf + 32 * half, tw = tl + TB_D + 128 * ob + 32 * half;
@@ -923,54 +1001,24 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 #pragma unroll
         for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
       }
-      operands_ready();
-      if (tid == 0) {
-        const uint64_t dut = layout_desc(UT, 0, 0);
-        const uint64_t daq = layout_desc(kmajor(rb + REC_AQ, 0), 0, 0);
-        const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
-#pragma unroll
-        for (int k0 = 0; k0 < CH; k0 += 16) {
-          const uint64_t a = desc_adv(dut, k0, false);
-          umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);      // M6
-          umma_bf16(td + 64, a, desc_adv(daq, k0, false), ID_O2, 1);        // M5, second half
-        }
-        umma_commit(bar_mma);
-        umma_commit(&o_full[ob]);
-      }
-      if (!(ok = wait_chain(bar_mma, mma_phase))) break;
-      mma_phase ^= 1u;
-      const bool more = j + 1 < nchunks;
-      if (j + 2 < nchunks) {  // this buffer is consumed: fetch chunk j + 2 into it
-        if (tid == 0) {
-          fence_proxy_async_smem();
-          issue_loads(j + 2, buf);
-        }
-        ++pending;
-      }
-      if (more) {
-        if (!(ok = wait_chain(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
-        --pending;
-        if (tid == 0) issue_m3(j + 1);  // runs under the rebuild below
-      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(ut_ready);
+      if (!(ok = mbar_wait(mma_b, j & 1))) break;
+      tc_fence_after_sync();
       {  // the fp16 state operand for the next chunk (and the final state)
         float sv[64];
         tmem_ld64(tl + TB_S + 64 * half, sv);
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 8) st8h(layout_addr(ST, v, c_lo + c0), sv + c0);
-        if (!more && p.s1 && v < DIN) {  // final state S[c][v] = S^T[v][c]
+        if (j + 1 == nchunks && s_out && v < DIN) {  // S[c][v] = S^T[v][c]
 #pragma unroll
           for (int c0 = 0; c0 < 64; ++c0)
-            if (c_lo + c0 < DIN) p.s1[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
+            if (c_lo + c0 < DIN) s_out[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
         }
       }
     }
-    if (ok && nchunks == 0 && p.s1 && v < DIN) {  // no tokens: final state = initial state
-      for (int c = c_lo; c < c_lo + 64 && c < DIN; ++c)
-        p.s1[sbase + (size_t)c * DIN + v] = p.s0 ? p.s0[sbase + (size_t)c * DIN + v] : 0.f;
-    }
-    if (!ok && tid == 0) {  // let copies already issued land before the CTA's memory goes away
-      for (int j = 0; j < 2 && pending > 0; ++j, --pending) mbar_wait(&full[j], 0, 100000000ull);
-    }
+    if (!ok) fail();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -978,8 +1026,10 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 }
 
 // Packed sequences: chunk_base[n] = sum_{m < n} ceil(len_m / 64), n = 0..N.
+// A negative length, or one above the caller's max_len (the work list is
+// sized by it), is reported as an invalid argument in the status word.
 __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ cu, int N,
-                                                        int* __restrict__ chunk_base) {
+                                                        int max_len, int* __restrict__ chunk_base) {
   __shared__ int warp_tot[32];
   __shared__ int carry_s;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -990,7 +1040,7 @@ __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ 
     int cnt = 0;
     if (i < N) {
       const int len = cu[i + 1] - cu[i];
-      if (len < 0) set_status(1);
+      if (len < 0 || len > max_len) set_status(1);
       cnt = len > 0 ? (len + CH - 1) / CH : 0;
     }
     int x = cnt;  // inclusive warp scan
@@ -1024,33 +1074,151 @@ cudaError_t set_smem(K kern, uint32_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Per-device launch context: the SM count and, for the segmented schedule,
+// two internal streams (stage 1 at low priority, stage 2 at high) and the
+// events that fork them from and join them back to the caller's stream.
+struct DeviceCtx {
+  bool ready = false;
+  int sms = 0;
+  cudaStream_t lo = nullptr, hi = nullptr;
+  cudaEvent_t fork = nullptr, seg = nullptr, join = nullptr;
+};
+std::mutex g_ctx_mu;
+DeviceCtx g_ctx[64];
+
+cudaError_t device_ctx(DeviceCtx** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DeviceCtx& c = g_ctx[dev];
+  if (!c.ready) {
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.lo, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.hi, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.seg, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    c.ready = true;
+  }
+  *out = &c;
+  return cudaSuccess;
+}
+
+// Chunks per segment of the overlapped schedule: about eight segments, a
+// multiple of 16 chunks, at least 32.
+int segment_chunks(int nc_max) {
+  const int s = (nc_max + 7) / 8;
+  return s < 32 ? 32 : (s + 15) / 16 * 16;
+}
+
+// The overlapped schedule pays off for long sequences and few states:
+// below 512 chunks its fill and drain cost more than the overlap gains, and
+// stage 2 must leave stage 1 at least half the SMs.
+bool use_overlap(int n_states, int nc_max, int sms) {
+  return n_states <= sms / 2 && nc_max >= 512;
+}
+
 template <int DIN, typename OutT>
 cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tg, int* chunk_base,
-                          uint8_t* records, int grid_chunks, cudaStream_t stream) {
+                          uint8_t* records, float* carry, int nc_max, bool allow_overlap,
+                          cudaStream_t stream) {
   // the shared-memory opt-in is a per-device function attribute; setting it
   // on every call costs next to nothing
-  cudaError_t e = set_smem(kda_intra_kernel<DIN, false>, A_SMEM);
-  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true>, A_SMEM);
+  cudaError_t e = set_smem(kda_intra_kernel<DIN, false, true>, A_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true, true>, A_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, false, false>, A_SMEM_ONE);
+  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true, false>, A_SMEM_ONE);
   if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
   if (e != cudaSuccess) return e;
-  IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
-                 pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0};
-  const dim3 grid((unsigned)grid_chunks, (unsigned)pr.H);
-  if (pr.diag_per_pair)
-    kda_intra_kernel<DIN, true><<<grid, 128, A_SMEM, stream>>>(tq, tk, tg, ip);
-  else
-    kda_intra_kernel<DIN, false><<<grid, 128, A_SMEM, stream>>>(tq, tk, tg, ip);
-  e = cudaGetLastError();
+  DeviceCtx* ctx = nullptr;
+  std::lock_guard<std::mutex> lock(g_ctx_mu);
+  e = device_ctx(&ctx);
   if (e != cudaSuccess) return e;
-  StateParams sp{records, pr.initial_state, pr.final_state, pr.out, pr.cu_seqlens, chunk_base,
-                 pr.T, pr.n_seq, pr.H, pr.scale};
-  kda_state_kernel<DIN, OutT>
-      <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
-  return cudaGetLastError();
+  const int n_states = pr.n_seq * pr.H;
+
+  // ctas > 0: persistent launch on that many SMs; ctas == 0: one CTA per item
+  auto intra = [&](int j_lo, int seg_len, int ctas, cudaStream_t st) -> cudaError_t {
+    const long long items = (long long)pr.n_seq * seg_len * pr.H;
+    IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
+                   pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items};
+    if (ctas > 0) {
+      const int grid = (int)std::min<long long>((items + 1) / 2, ctas);
+      if (pr.diag_per_pair)
+        kda_intra_kernel<DIN, true, true><<<grid, A_THREADS, A_SMEM, st>>>(tq, tk, tg, ip);
+      else
+        kda_intra_kernel<DIN, false, true><<<grid, A_THREADS, A_SMEM, st>>>(tq, tk, tg, ip);
+    } else {
+      if (pr.diag_per_pair)
+        kda_intra_kernel<DIN, true, false><<<(unsigned)items, 128, A_SMEM_ONE, st>>>(tq, tk, tg, ip);
+      else
+        kda_intra_kernel<DIN, false, false><<<(unsigned)items, 128, A_SMEM_ONE, st>>>(tq, tk, tg, ip);
+    }
+    return cudaGetLastError();
+  };
+  auto state = [&](int j_lo, int j_hi, cudaStream_t st) -> cudaError_t {
+    StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, pr.cu_seqlens,
+                   chunk_base, pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale};
+    kda_state_kernel<DIN, OutT>
+        <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, st>>>(tv, sp);
+    return cudaGetLastError();
+  };
+
+  // Overlapped schedule: stage 1 of segment s + 1 runs while stage 2 walks
+  // segment s.  Stage 1 is left n_states SMs short, so the stage-2 CTAs (one
+  // per sequence and head, a whole SM each) always find room.  Stage 2 of a
+  // segment starts only after stage 1 of that segment has finished (an
+  // event); no kernel waits on another on the device.
+  const int seg = segment_chunks(nc_max);
+  const bool overlap = allow_overlap && carry && use_overlap(n_states, nc_max, ctx->sms);
+  if (!overlap) {
+    e = intra(0, nc_max, 0, stream);
+    if (e == cudaSuccess) e = state(0, nc_max, stream);
+    return e;
+  }
+  const int intra_ctas = ctx->sms - n_states;
+  e = cudaEventRecord(ctx->fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->lo, ctx->fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->hi, ctx->fork, 0);
+  for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
+    const int len = std::min(seg, nc_max - j_lo);
+    e = intra(j_lo, len, intra_ctas, ctx->lo);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->seg, ctx->lo);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->hi, ctx->seg, 0);
+    if (e == cudaSuccess) e = state(j_lo, j_lo + len, ctx->hi);
+  }
+  // every stage-1 launch precedes a stage-2 launch on hi, so joining hi is enough
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->join, ctx->hi);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ctx->join, 0);
+  return e;
 }
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
+  DeviceCtx* ctx = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_ctx_mu);
+    if (device_ctx(&ctx) != cudaSuccess) return -1;
+  }
+  const int nc_max = (max_len + CH - 1) / CH;
+  if (n_seq <= 0 || nc_max <= 0 || H <= 0) return 0;
+  const int plan = packed ? 1 : 0;
+  if (!use_overlap(n_seq * H, nc_max, ctx->sms)) return plan + 2;
+  const int seg = segment_chunks(nc_max);
+  return plan + 2 * ((nc_max + seg - 1) / seg);
+}
+
+namespace {
+
+size_t plan_bytes(int n_seq) { return align_up((size_t)(n_seq + 1) * sizeof(int), 1024); }
+size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float); }
 
 }  // namespace
 
@@ -1059,41 +1227,28 @@ size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H
   size_t plan = 0;
   if (packed) {
     chunks = T_or_total / CH + n_seq;  // sum of ceil(len / 64) is at most this
-    plan = align_up((size_t)(n_seq + 1) * sizeof(int), 1024);
+    plan = plan_bytes(n_seq);
   } else {
     chunks = (long long)n_seq * ((T_or_total + CH - 1) / CH);
   }
-  return plan + (size_t)chunks * H * REC_BYTES;
+  return plan + carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
 }
 
-cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream_t stream) {
+namespace {
+
+// records: per-(chunk, head) records; carry: the state between segments (or
+// null, which forces a single segment).
+cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, uint8_t* records,
+                        bool allow_overlap, cudaStream_t stream) {
   const uint64_t d = (uint64_t)pr.d, H = (uint64_t)pr.H;
-  if (pr.T_total == 0) {
-    // no tokens at all: the final state is the initial state
-    if (!pr.final_state) return cudaSuccess;
-    const size_t bytes = (size_t)pr.n_seq * pr.H * pr.d * pr.d * sizeof(float);
-    if (pr.initial_state)
-      return pr.initial_state == pr.final_state
-                 ? cudaSuccess
-                 : cudaMemcpyAsync(pr.final_state, pr.initial_state, bytes,
-                                   cudaMemcpyDeviceToDevice, stream);
-    return cudaMemsetAsync(pr.final_state, 0, bytes, stream);
-  }
   const bool packed = pr.cu_seqlens != nullptr;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* chunk_base = nullptr;
-  int grid_chunks;
   if (packed) {
-    chunk_base = reinterpret_cast<int*>(ws);
-    ws += align_up((size_t)(pr.n_seq + 1) * sizeof(int), 1024);
-    kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, chunk_base);
+    kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, pr.T, chunk_base);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    grid_chunks = pr.T_total / CH + pr.n_seq;
-  } else {
-    grid_chunks = pr.n_seq * ((pr.T + CH - 1) / CH);
   }
-  if (grid_chunks == 0) return cudaSuccess;
+  const int nc_max = (pr.T + CH - 1) / CH;  // T is max_seqlen when packed
+  if (nc_max == 0) return cudaSuccess;
   const uint64_t rows = (uint64_t)pr.T_total;
   CUtensorMap tq, tk, tv, tg;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -1103,12 +1258,41 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream
       !make_map_3d_bf16(&tg, pr.log_alpha, d, H, rows, d, H * d, 64, 1, 64, sw))
     return cudaErrorInvalidValue;
   if (pr.d == 128)
-    return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, chunk_base, ws, grid_chunks, stream)
-                      : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, ws,
-                                                          grid_chunks, stream);
-  return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, ws, grid_chunks, stream)
-                    : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, ws,
-                                                       grid_chunks, stream);
+    return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
+                                                  nc_max, allow_overlap, stream)
+                      : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
+                                                          carry, nc_max, allow_overlap, stream);
+  return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
+                                               nc_max, allow_overlap, stream)
+                    : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
+                                                       carry, nc_max, allow_overlap, stream);
+}
+
+// The caller's problem has no tokens at all: the final state is the initial state.
+cudaError_t copy_initial_state(const ChunkProblem& pr, cudaStream_t stream) {
+  if (!pr.final_state) return cudaSuccess;
+  const size_t bytes = (size_t)pr.n_seq * pr.H * pr.d * pr.d * sizeof(float);
+  if (pr.initial_state)
+    return pr.initial_state == pr.final_state
+               ? cudaSuccess
+               : cudaMemcpyAsync(pr.final_state, pr.initial_state, bytes,
+                                 cudaMemcpyDeviceToDevice, stream);
+  return cudaMemsetAsync(pr.final_state, 0, bytes, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream_t stream) {
+  if (pr.T_total == 0) return copy_initial_state(pr, stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* chunk_base = nullptr;
+  if (pr.cu_seqlens) {
+    chunk_base = reinterpret_cast<int*>(ws);
+    ws += plan_bytes(pr.n_seq);
+  }
+  float* carry = reinterpret_cast<float*>(ws);
+  ws += carry_bytes(pr.n_seq, pr.H);
+  return launch_impl(pr, chunk_base, carry, ws, true, stream);
 }
 
 // ---- allocation-free variant --------------------------------------------
@@ -1144,7 +1328,9 @@ cudaError_t launch_chunk_fwd_noalloc(const ChunkProblem& pr, cudaStream_t stream
     }
     scratch = addr[dev];
   }
-  return launch_chunk_fwd(pr, scratch, stream);
+  if (pr.T_total == 0) return copy_initial_state(pr, stream);
+  // one segment (no carried state, no internal streams), records only
+  return launch_impl(pr, nullptr, nullptr, static_cast<uint8_t*>(scratch), false, stream);
 }
 
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err) {

@@ -39,6 +39,9 @@ size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 
+// Kernel launches one prefill call of this shape makes on the current device.
+int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H);
+
 // Same path with the library's fixed device scratch instead of a caller
 // workspace (fixed-length problems of at most noalloc_max_records() records).
 size_t noalloc_max_records();

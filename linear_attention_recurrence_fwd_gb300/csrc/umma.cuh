@@ -282,6 +282,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // Untiled bulk copies (addresses 16-byte aligned, size a multiple of 16).
+// Warm L2 with a tile ahead of its shared-memory load (no completion to
+// wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_global, uint32_t bytes,
                                          uint64_t* bar) {
   asm volatile(
@@ -306,6 +314,10 @@ __device__ __forceinline__ void bulk_wait_all() {
 // Wait until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_reads() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed bulk group but the most recent one is done reading shared memory.
+__device__ __forceinline__ void bulk_wait_reads_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- misc
