@@ -86,10 +86,10 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
  *                     each) passed from the intra-chunk stage to the state
  *                     pass, and the fp32 state handed between segments of
  *                     the sequence.  Too small or NULL -> KDA_ERR_WORKSPACE.
- * Long sequences run as segments of chunks: the intra-chunk stage of one
- * segment overlaps the state pass of the previous one on two internal
- * streams (created once per device), forked from and joined back to
- * `stream` with events, so the call stays ordered on `stream`.
+ * Long sequences run as segments of chunks, all on `stream`: the
+ * intra-chunk stage of one segment is a programmatic dependent launch of
+ * the previous segment's state pass and runs on the SMs that pass leaves
+ * free.
  * The chunked evaluation (64-token chunks of four 16-token tiles) follows
  * the blockwise computation the orkas.ai page describes in section "Eine
  * Untergrenze, die einen GPU-Codepfad beseitigte".  out must not alias any
@@ -104,7 +104,7 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
                            cudaStream_t stream);
 
 /* Bytes of device workspace kda_chunk_fwd needs for this shape:
- * B * ceil(T / 64) * H * 66560 + B * H * 65536. */
+ * B * ceil(T / 64) * H * 66560 + B * H * 65536 + 256. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /* Kernel launches one kda_chunk_fwd call of this shape makes on the current
@@ -167,8 +167,8 @@ KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             float scale, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
-/* (T_total / 64 + N) * H * 66560 + N * H * 65536, plus 4 (N + 1) bytes
- * rounded up to 1 KiB. */
+/* (T_total / 64 + N) * H * 66560 + N * H * 65536 + 256, plus 4 (N + 1)
+ * bytes rounded up to 1 KiB. */
 KDA_API size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v);
 
 /*

@@ -93,10 +93,7 @@ constexpr uint32_t A_WST = 81920;                         // W record image     
 constexpr uint32_t A_TI = 0;                              // T fp32 (in the W slot, before W)
 constexpr uint32_t A_DINV = 57344;                        // T_aa transposed, 4 KB (in the T diag(beta) slot, before it)
 constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
-constexpr uint32_t A_SLOT = A_MISC + 1024;                // one slot's shared memory
-constexpr uint32_t A_SMEM = 2 * A_SLOT + 1024;            // two slots + alignment slack
-constexpr int A_THREADS = 256;                            // two slots of 128 threads
-constexpr uint32_t A_SMEM_ONE = A_SLOT + 1024;            // one slot (one item per CTA)
+constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
 
 // ---- stage 2 shared memory
 constexpr uint32_t B_REC0 = 0, B_V0 = 66560, B_REC1 = 82944, B_V1 = 149504;
@@ -106,8 +103,7 @@ constexpr uint32_t B_MISC = 215040;
 constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
-constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0;  // within a slot
-constexpr uint32_t TA_SLOT_COLS = 256, TA_COLS = 512;
+constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
 // Stage 2: U~ (M3 result, two buffers), D = [-S^T W^T | -O^T] (two buffers of
 // 128 columns: the U correction and the output share one N = 128 product)
 // and the fp32 state S^T.
@@ -216,12 +212,6 @@ __device__ __forceinline__ void build_version(const OperandLayout& XH, const Ope
   }
 }
 
-// Stage 1 runs two independent items per CTA ("slots", 128 threads each);
-// a slot synchronises on its own named barrier (1 or 2).
-__device__ __forceinline__ void slot_sync(int slot) {
-  asm volatile("bar.sync %0, 128;" ::"r"(slot + 1) : "memory");
-}
-
 // T (fp32 64x64) with 16-byte chunks XOR-swizzled by row.
 __device__ __forceinline__ int tix(int r, int c) {
   return r * CH + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
@@ -232,7 +222,7 @@ __device__ __forceinline__ int tix(int r, int c) {
 // = T_aa[rr][x]; P goes to the unused upper-triangle block (b, a) of ti.
 template <int S>
 __device__ __forceinline__ void solve_level(const float* akk, float* ti, const float* dinv,
-                                            int tid, int slot) {
+                                            int tid) {
   constexpr int kStrips = (4 - S) * 64;  // (block, row, 4-column quad)
 #pragma unroll
   for (int st = tid; st < kStrips; st += 128) {
@@ -254,7 +244,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
     *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) =
         make_float4(acc0, acc1, acc2, acc3);
   }
-  slot_sync(slot);
+  __syncthreads();
 #pragma unroll
   for (int st = tid; st < kStrips; st += 128) {
     const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
@@ -271,7 +261,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
     *reinterpret_cast<float4*>(ti + tix(16 * a + rr, 16 * b + 4 * q)) =
         make_float4(-acc0, -acc1, -acc2, -acc3);
   }
-  slot_sync(slot);
+  __syncthreads();
 }
 
 // Ablation of the dense diagonal tiles: the four 16x16 diagonal tiles of
@@ -285,8 +275,8 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
 // which is free once M1 is done; one thread per position pair walks the
 // channels starting at a thread-dependent offset so a warp's loads fall in
 // distinct banks.  res[0..1023] receives A_qk and res[1024..2047] A_kk, as
-// [tile][r % 16][i % 16].  Called by all 128 threads of a slot.
-__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid, int slot,
+// [tile][r % 16][i % 16].  Called by all 128 threads of the CTA.
+__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
                                                      float* res) {
   uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
   uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
@@ -306,7 +296,7 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
       sg[(t0 + j) * DP + c] = gv[j];
     }
   }
-  slot_sync(slot);
+  __syncthreads();
 #pragma unroll 1
   for (int pidx = tid; pidx < 4 * 136; pidx += 128) {
     const int a = pidx / 136, idx = pidx - 136 * a;
@@ -326,7 +316,7 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
     res[(16 * a + rr) * 16 + ii] = aq;
     res[1024 + (16 * a + rr) * 16 + ii] = ak;
   }
-  slot_sync(slot);
+  __syncthreads();
 }
 
 // Stage 1 work list: item w = ((n * seg_len) + (j - j_lo)) * H + h covers
@@ -339,28 +329,24 @@ struct IntraParams {
   int T, n_seq, H;
   int check_decay;
   int j_lo, seg_len, n_items;
+  int* grid_done;  // launched as a dependent of a state pass: CTAs finished, else null
 };
 
-template <int DIN, bool PAIRS, bool PERSIST>
-__global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
+template <int DIN, bool PAIRS>
+__global__ void __launch_bounds__(128, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
-  // PERSIST: each CTA holds one SM (two slots' shared memory) and its two
-  // slots walk the work list independently, so a launch that leaves some SMs
-  // out leaves them entirely free.  Otherwise one CTA (one slot) per item,
-  // two CTAs per SM.
+  // One CTA per item (chunk, head), two CTAs per SM.  The item loop also
+  // covers a grid smaller than the work list.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  constexpr uint32_t kCols = PERSIST ? TA_COLS : TA_SLOT_COLS;
-  const int slot = PERSIST ? threadIdx.x >> 7 : 0;
-  const int tid = threadIdx.x & 127, warp = tid >> 5;  // within the slot
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int H = p.H;
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb0 = (raw + 1023u) & ~1023u;
-  const uint32_t sb = sb0 + (uint32_t)slot * A_SLOT;
+  const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sbp = smem_raw + (sb - raw);
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sbp + A_MISC);
   uint64_t* bar_mma = bar_tma + 1;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem_raw + (sb0 - raw) + A_MISC + 16);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + A_MISC + 16);
   int* s_abort = reinterpret_cast<int*>(sbp + A_MISC + 20);
   float* s_beta = reinterpret_cast<float*>(sbp + A_MISC + 64);    // [64]
   float* s_gamma = reinterpret_cast<float*>(sbp + A_MISC + 512);  // [128], 16-byte aligned
@@ -371,15 +357,14 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     mbar_fence_init();
     *s_abort = 0;
   }
-  if (threadIdx.x < 32) {
-    tmem_alloc(tmem_base_s, kCols);
+  if (warp == 0) {
+    tmem_alloc(tmem_base_s, TA_COLS);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_all = *tmem_base_s;
-  const uint32_t tmem = tmem_all + TA_SLOT_COLS * (uint32_t)slot;
+  const uint32_t tmem = *tmem_base_s;
   const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
   uint32_t tma_phase = 0, mma_phase = 0;
   bool ok = true;
@@ -390,14 +375,14 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
       set_status(6);
     }
     phase ^= 1u;
-    slot_sync(slot);
+    __syncthreads();
     tc_fence_after_sync();
     return *s_abort == 0;
   };
   auto operands_ready = [&]() {
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    slot_sync(slot);
+    __syncthreads();
     tc_fence_after_sync();
   };
 
@@ -425,9 +410,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     it.valid = min(CH, len - CH * jc);
     return it;
   };
-  const int stride = PERSIST ? 2 * (int)gridDim.x : (int)gridDim.x;
-  for (int w = PERSIST ? 2 * (int)blockIdx.x + slot : (int)blockIdx.x; ok && w < p.n_items;
-       w += stride) {
+  for (int w = blockIdx.x; ok && w < p.n_items; w += gridDim.x) {
   const Item cur = item_of(w);
   if (cur.valid <= 0) continue;
   const int h = cur.h, t0 = cur.t0, valid = cur.valid, qrec = cur.qrec;
@@ -447,7 +430,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     }
   }
   const float beta_t = tid < valid ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-  slot_sync(slot);
+  __syncthreads();
   if (DIN == 64) {  // upper channel half of the raw tiles stays zero
     for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
       st_shared_v4(sb + A_RQ + 8192 + off, 0, 0, 0, 0);
@@ -475,7 +458,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
   if (tid < CH) s_beta[tid] = beta_t;
   fence_proxy_async_smem();
   tc_fence_before_sync();
-  slot_sync(slot);
+  __syncthreads();
   tc_fence_after_sync();
 
   ok = wait_all(bar_tma, tma_phase);
@@ -531,7 +514,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
   // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
   // M1 operands below overwrite
   if (tid == 0) bulk_wait_reads();
-  slot_sync(slot);
+  __syncthreads();
   if (ok) {
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -574,7 +557,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
 
   // per-pair diagonal tiles (ablation only), kept in the (k e^g)^T slot
   float* s_pair = reinterpret_cast<float*>(sbp + A_KT);
-  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, slot, s_pair);
+  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, s_pair);
 
   float* akk = reinterpret_cast<float*>(sbp + A_AKK);
   float* ti = reinterpret_cast<float*>(sbp + A_TI);
@@ -612,7 +595,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
         for (int i = 0; i < CH; ++i) akk[i * CH + r] = (i < r) ? br * a[i] : 0.f;
       }
     }
-    if (PAIRS) slot_sync(slot);  // s_pair is overwritten by (k e^g)^T below
+    if (PAIRS) __syncthreads();  // s_pair is overwritten by (k e^g)^T below
     // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -639,7 +622,7 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     }
     s_gamma[c] = GE[3];
     fence_proxy_async_smem();
-    slot_sync(slot);
+    __syncthreads();
     if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
       bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
       bulk_commit();
@@ -667,12 +650,12 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
 #pragma unroll
       for (int q = 0; q < 4; ++q) drow[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
-    slot_sync(slot);
+    __syncthreads();
     // off-diagonal blocks by distance s = a - b: P = sum_{m=b}^{a-1} L_am T_mb,
     // then T_ab = -T_aa P.  A thread owns a strip of 4 columns of one row.
-    solve_level<1>(akk, ti, dinv, tid, slot);
-    solve_level<2>(akk, ti, dinv, tid, slot);
-    solve_level<3>(akk, ti, dinv, tid, slot);
+    solve_level<1>(akk, ti, dinv, tid);
+    solve_level<2>(akk, ti, dinv, tid);
+    solve_level<3>(akk, ti, dinv, tid);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
       const int r = tid >> 1, i_lo = (tid & 1) * 32;
@@ -702,13 +685,13 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
     ok = wait_all(bar_mma, mma_phase);
   }
   if (ok) {
-    // ---- W (fp16, N = r, K = c) from W^T in TMEM (lane = c), into the T slot
+    // ---- W (fp16, N = r, K = c) from W^T in TMEM (lane = c), into the (k e^g)^T slot
     float w[64];
     tmem_ld64(tl + TA_W, w);
 #pragma unroll
     for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(WT, r0, c), w + r0);
     fence_proxy_async_smem();
-    slot_sync(slot);
+    __syncthreads();
     if (tid == 0) {
       bulk_s2g(rec + REC_WT, sb + A_WST, REC_QT - REC_WT);
       bulk_s2g(rec + REC_TB, sb + A_STG + REC_TB, REC_G - REC_TB);
@@ -720,7 +703,18 @@ __global__ void __launch_bounds__(PERSIST ? A_THREADS : 128, PERSIST ? 1 : 2)
   if (tid == 0) bulk_wait_all();
   tc_fence_before_sync();
   __syncthreads();
-  if (threadIdx.x < 32) tmem_dealloc(tmem_all, kCols);
+  if (warp == 0) tmem_dealloc(tmem, TA_COLS);
+  if (p.grid_done && threadIdx.x == 0) {
+    // This grid was allowed to start before the previous segment's state
+    // pass finished.  The CTA that finishes last waits for that grid, so
+    // this grid completes only after it: the next state pass, which reads
+    // the state it carried, is ordered after both.
+    const int ticket = atomicAdd(p.grid_done, 1);
+    if (ticket == (int)(gridDim.x * gridDim.y) - 1) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      *p.grid_done = 0;
+    }
+  }
 }
 
 // Stage 2 covers chunks [j_lo, j_hi) of every sequence.  The state entering
@@ -753,6 +747,9 @@ constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
 template <int DIN, typename OutT>
 __global__ void __launch_bounds__(B_THREADS, 1)
     kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
+  // Every CTA of this grid holds its SM from here on: the next segment's
+  // intra-chunk stage (a programmatic dependent) may start on the other SMs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int half = (warp >> 2) & 1;           // chain warps: which half of the columns
@@ -1076,37 +1073,20 @@ cudaError_t set_smem(K kern, uint32_t bytes) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Per-device launch context: the SM count and, for the segmented schedule,
-// two internal streams (stage 1 at low priority, stage 2 at high) and the
-// events that fork them from and join them back to the caller's stream.
-struct DeviceCtx {
-  bool ready = false;
-  int sms = 0;
-  cudaStream_t lo = nullptr, hi = nullptr;
-  cudaEvent_t fork = nullptr, seg = nullptr, join = nullptr;
-};
-std::mutex g_ctx_mu;
-DeviceCtx g_ctx[64];
-
-cudaError_t device_ctx(DeviceCtx** out) {
+// SM count of the current device, cached per device.
+int g_sms[64];
+std::mutex g_sms_mu;
+cudaError_t device_sms(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  DeviceCtx& c = g_ctx[dev];
-  if (!c.ready) {
-    int least = 0, greatest = 0;
-    e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.lo, cudaStreamNonBlocking, least);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&c.hi, cudaStreamNonBlocking, greatest);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.seg, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
+  std::lock_guard<std::mutex> lock(g_sms_mu);
+  if (!g_sms[dev]) {
+    e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    c.ready = true;
   }
-  *out = &c;
+  *sms = g_sms[dev];
   return cudaSuccess;
 }
 
@@ -1127,90 +1107,80 @@ bool use_overlap(int n_states, int nc_max, int sms) {
 template <int DIN, typename OutT>
 cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tg, int* chunk_base,
-                          uint8_t* records, float* carry, int nc_max, bool allow_overlap,
-                          cudaStream_t stream) {
+                          uint8_t* records, float* carry, int* grid_done, int nc_max,
+                          bool allow_overlap, cudaStream_t stream) {
   // the shared-memory opt-in is a per-device function attribute; setting it
   // on every call costs next to nothing
-  cudaError_t e = set_smem(kda_intra_kernel<DIN, false, true>, A_SMEM);
-  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true, true>, A_SMEM);
-  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, false, false>, A_SMEM_ONE);
-  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true, false>, A_SMEM_ONE);
+  cudaError_t e = set_smem(kda_intra_kernel<DIN, false>, A_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true>, A_SMEM);
   if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
   if (e != cudaSuccess) return e;
-  DeviceCtx* ctx = nullptr;
-  std::lock_guard<std::mutex> lock(g_ctx_mu);
-  e = device_ctx(&ctx);
+  int sms = 0;
+  e = device_sms(&sms);
   if (e != cudaSuccess) return e;
-  const int n_states = pr.n_seq * pr.H;
 
-  // ctas > 0: persistent launch on that many SMs; ctas == 0: one CTA per item
-  auto intra = [&](int j_lo, int seg_len, int ctas, cudaStream_t st) -> cudaError_t {
+  // One CTA per item, two per SM.  dependent: a programmatic dependent launch
+  // of the state pass just enqueued (it may start once that grid's CTAs are
+  // all resident).
+  auto intra = [&](int j_lo, int seg_len, bool dependent) -> cudaError_t {
     const long long items = (long long)pr.n_seq * seg_len * pr.H;
     IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
-                   pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items};
-    if (ctas > 0) {
-      const int grid = (int)std::min<long long>((items + 1) / 2, ctas);
-      if (pr.diag_per_pair)
-        kda_intra_kernel<DIN, true, true><<<grid, A_THREADS, A_SMEM, st>>>(tq, tk, tg, ip);
-      else
-        kda_intra_kernel<DIN, false, true><<<grid, A_THREADS, A_SMEM, st>>>(tq, tk, tg, ip);
-    } else {
-      if (pr.diag_per_pair)
-        kda_intra_kernel<DIN, true, false><<<(unsigned)items, 128, A_SMEM_ONE, st>>>(tq, tk, tg, ip);
-      else
-        kda_intra_kernel<DIN, false, false><<<(unsigned)items, 128, A_SMEM_ONE, st>>>(tq, tk, tg, ip);
-    }
-    return cudaGetLastError();
+                   pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items,
+                   dependent ? grid_done : nullptr};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)items);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = A_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return pr.diag_per_pair ? cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, true>, tq, tk, tg, ip)
+                            : cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, false>, tq, tk, tg, ip);
   };
-  auto state = [&](int j_lo, int j_hi, cudaStream_t st) -> cudaError_t {
+  auto state = [&](int j_lo, int j_hi) -> cudaError_t {
     StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, pr.cu_seqlens,
                    chunk_base, pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale};
     kda_state_kernel<DIN, OutT>
-        <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, st>>>(tv, sp);
+        <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
     return cudaGetLastError();
   };
 
-  // Overlapped schedule: stage 1 of segment s + 1 runs while stage 2 walks
-  // segment s.  Stage 1 is left n_states SMs short, so the stage-2 CTAs (one
-  // per sequence and head, a whole SM each) always find room.  Stage 2 of a
-  // segment starts only after stage 1 of that segment has finished (an
-  // event); no kernel waits on another on the device.
-  const int seg = segment_chunks(nc_max);
-  const bool overlap = allow_overlap && carry && use_overlap(n_states, nc_max, ctx->sms);
+  // Overlapped schedule, all on the caller's stream: segments of chunks,
+  //   intra(0), state(0), intra(1)*, state(1), intra(2)*, ...
+  // where * marks a programmatic dependent launch.  A state pass holds one
+  // SM per (sequence, head) and lets the next segment's intra-chunk stage
+  // fill the other SMs while it runs; that stage's grid completes only after
+  // the state pass (its last CTA waits for it), so every state pass starts
+  // after both the records of its segment and the state carried into it.
+  const bool overlap = allow_overlap && carry && grid_done &&
+                       use_overlap(pr.n_seq * pr.H, nc_max, sms);
   if (!overlap) {
-    e = intra(0, nc_max, 0, stream);
-    if (e == cudaSuccess) e = state(0, nc_max, stream);
+    e = intra(0, nc_max, false);
+    if (e == cudaSuccess) e = state(0, nc_max);
     return e;
   }
-  const int intra_ctas = ctx->sms - n_states;
-  e = cudaEventRecord(ctx->fork, stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->lo, ctx->fork, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->hi, ctx->fork, 0);
+  const int seg = segment_chunks(nc_max);
+  e = cudaMemsetAsync(grid_done, 0, sizeof(int), stream);
   for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
     const int len = std::min(seg, nc_max - j_lo);
-    e = intra(j_lo, len, intra_ctas, ctx->lo);
-    if (e == cudaSuccess) e = cudaEventRecord(ctx->seg, ctx->lo);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->hi, ctx->seg, 0);
-    if (e == cudaSuccess) e = state(j_lo, j_lo + len, ctx->hi);
+    e = intra(j_lo, len, j_lo > 0);
+    if (e == cudaSuccess) e = state(j_lo, j_lo + len);
   }
-  // every stage-1 launch precedes a stage-2 launch on hi, so joining hi is enough
-  if (e == cudaSuccess) e = cudaEventRecord(ctx->join, ctx->hi);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ctx->join, 0);
   return e;
 }
 
 }  // namespace
 
 int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
-  DeviceCtx* ctx = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_ctx_mu);
-    if (device_ctx(&ctx) != cudaSuccess) return -1;
-  }
+  int sms = 0;
+  if (device_sms(&sms) != cudaSuccess) return -1;
   const int nc_max = (max_len + CH - 1) / CH;
   if (n_seq <= 0 || nc_max <= 0 || H <= 0) return 0;
   const int plan = packed ? 1 : 0;
-  if (!use_overlap(n_seq * H, nc_max, ctx->sms)) return plan + 2;
+  if (!use_overlap(n_seq * H, nc_max, sms)) return plan + 2;
   const int seg = segment_chunks(nc_max);
   return plan + 2 * ((nc_max + seg - 1) / seg);
 }
@@ -1218,7 +1188,8 @@ int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
 namespace {
 
 size_t plan_bytes(int n_seq) { return align_up((size_t)(n_seq + 1) * sizeof(int), 1024); }
-size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float); }
+// carried states, then 256 bytes for the finished-CTA counter of the overlapped schedule
+size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float) + 256; }
 
 }  // namespace
 
@@ -1238,8 +1209,8 @@ namespace {
 
 // records: per-(chunk, head) records; carry: the state between segments (or
 // null, which forces a single segment).
-cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, uint8_t* records,
-                        bool allow_overlap, cudaStream_t stream) {
+cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, int* grid_done,
+                        uint8_t* records, bool allow_overlap, cudaStream_t stream) {
   const uint64_t d = (uint64_t)pr.d, H = (uint64_t)pr.H;
   const bool packed = pr.cu_seqlens != nullptr;
   if (packed) {
@@ -1259,13 +1230,13 @@ cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, u
     return cudaErrorInvalidValue;
   if (pr.d == 128)
     return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
-                                                  nc_max, allow_overlap, stream)
+                                                  grid_done, nc_max, allow_overlap, stream)
                       : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
-                                                          carry, nc_max, allow_overlap, stream);
+                                                          carry, grid_done, nc_max, allow_overlap, stream);
   return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
-                                               nc_max, allow_overlap, stream)
+                                               grid_done, nc_max, allow_overlap, stream)
                     : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
-                                                       carry, nc_max, allow_overlap, stream);
+                                                       carry, grid_done, nc_max, allow_overlap, stream);
 }
 
 // The caller's problem has no tokens at all: the final state is the initial state.
@@ -1291,8 +1262,9 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream
     ws += plan_bytes(pr.n_seq);
   }
   float* carry = reinterpret_cast<float*>(ws);
+  int* grid_done = reinterpret_cast<int*>(ws + carry_bytes(pr.n_seq, pr.H) - 256);
   ws += carry_bytes(pr.n_seq, pr.H);
-  return launch_impl(pr, chunk_base, carry, ws, true, stream);
+  return launch_impl(pr, chunk_base, carry, grid_done, ws, true, stream);
 }
 
 // ---- allocation-free variant --------------------------------------------
@@ -1330,7 +1302,7 @@ cudaError_t launch_chunk_fwd_noalloc(const ChunkProblem& pr, cudaStream_t stream
   }
   if (pr.T_total == 0) return copy_initial_state(pr, stream);
   // one segment (no carried state, no internal streams), records only
-  return launch_impl(pr, nullptr, nullptr, static_cast<uint8_t*>(scratch), false, stream);
+  return launch_impl(pr, nullptr, nullptr, nullptr, static_cast<uint8_t*>(scratch), false, stream);
 }
 
 int read_and_clear_chunk_status(cudaStream_t stream, cudaError_t* err) {

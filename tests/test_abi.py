@@ -91,11 +91,11 @@ def test_workspace_sizes_are_queryable(lib):
 
 def test_chunk_workspace_is_required_and_sized(lib):
     need = lib.kda_chunk_fwd_workspace_size(2, 100, 3, 128, 128)
-    assert need == 2 * 2 * 3 * 66560 + 2 * 3 * 65536  # records + carried states
+    assert need == 2 * 2 * 3 * 66560 + 2 * 3 * 65536 + 256  # records, carried states, counter
     # valid shape, no workspace: rejected before anything is launched
     assert lib.kda_chunk_fwd(F, F, F, F, F, None, F, 1, None, 2, 100, 3, 128, 128, 1.0,
                              None, 0, None) == 7
     assert lib.kda_chunk_fwd(F, F, F, F, F, None, F, 1, None, 2, 100, 3, 128, 128, 1.0,
                              F, need - 16, None) == 7
     vneed = lib.kda_varlen_fwd_workspace_size(4, 1000, 2, 128, 128)
-    assert vneed == 1024 + (1000 // 64 + 4) * 2 * 66560 + 4 * 2 * 65536
+    assert vneed == 1024 + (1000 // 64 + 4) * 2 * 66560 + 4 * 2 * 65536 + 256
