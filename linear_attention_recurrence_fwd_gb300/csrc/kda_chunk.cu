@@ -42,10 +42,11 @@
 //   M2 (k e^g)^T (T diag beta)^T -> W^T.
 // The 64x64 unit lower-triangular inverse is formed in fp32 on CUDA cores.
 //
-// Precision.  The tile-referenced M1 operands span e^{+-80} and need bf16's
-// range; their 8-bit mantissa alone costs too much accuracy in A, so each is
-// split into a bf16 pair x = hi + lo and M1 accumulates hi.hi + lo.hi + hi.lo
-// (fp32 accumulation).  Every state-pass operand (S, W, q e^g, U, A_qk,
+// Precision.  The tile-referenced M1 operands span e^{+-80} and need an
+// 8-bit exponent; bf16's 8-bit mantissa alone costs too much accuracy in A,
+// so M1 runs as kind::tf32 on fp32 operands rounded to nearest tf32 (10
+// mantissa bits), K-major so that each thread (one key channel) writes one
+// element per row.  Every state-pass operand (S, W, q e^g, U, A_qk,
 // k e^{g_C - g}) is bounded by O(1)..O(10) and is stored as fp16 (3 more
 // mantissa bits than bf16, same tensor-core rate).  T diag(beta) and
 // (k e^g)^T pair with the raw bf16 v tile / each other and stay bf16.
@@ -84,8 +85,8 @@ constexpr uint32_t REC_BYTES = 66560;  // record stride
 // ---- stage 1 shared memory (bytes from a 1024-aligned base); phases reuse space
 constexpr uint32_t A_RQ = 0, A_RK = 16384, A_RG = 32768;  // raw TMA tiles   (transposes)
 constexpr uint32_t A_LM = 65536, A_IM = 73728;            // L, I (bf16)      (transposes)
-constexpr uint32_t A_XH = 0, A_XL = 32768;                // M1 A operand     (M1)
-constexpr uint32_t A_KBH = 65536, A_KBL = 81920;          // M1 B operand     (M1)
+constexpr uint32_t A_XH = 0;                              // M1 A operand, 64 KB (M1)
+constexpr uint32_t A_KBH = 65536;                         // M1 B operand, 32 KB (M1)
 constexpr uint32_t A_STG = 0;                             // record image [0, 64K) (after M1)
 constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][64]  (after M1)
 constexpr uint32_t A_KT = 81920;                          // (k e^g)^T bf16      (after M1)
@@ -151,18 +152,15 @@ __device__ __forceinline__ void st8h(uint32_t addr, const float* x) {
   st_shared_v4(addr, pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
                pack_f16x2(x[6], x[7]));
 }
-// x as an unevaluated bf16 pair: hi = bf16(x), lo = bf16(x - hi).  Each
-// packed hi pair is widened back with bit operations (bf16 -> fp32 is exact).
-__device__ __forceinline__ void st8_split(uint32_t addr_hi, uint32_t addr_lo, const float* x) {
-  uint32_t hi[4], lo[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-    const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xffff0000u);
-    lo[j] = pack_bf16x2(x[2 * j] - h0, x[2 * j + 1] - h1);
-  }
-  st_shared_v4(addr_hi, hi[0], hi[1], hi[2], hi[3]);
-  st_shared_v4(addr_lo, lo[0], lo[1], lo[2], lo[3]);
+// x rounded to nearest tf32 (10 explicit mantissa bits), as the bit pattern
+// of an fp32 whose low 13 bits are zero.
+__device__ __forceinline__ float tf32r(float x) {
+  uint32_t y;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+  return __uint_as_float(y);
+}
+__device__ __forceinline__ void st_f32(uint32_t addr, float x) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -185,11 +183,11 @@ __device__ __forceinline__ void set_status(int code) { atomicExch(&g_chunk_statu
 
 // Version b of the M1 A operand: rows r >= 16 b of [Q^(b); K^(b)] with
 // Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r F[tile(r)][b] (same for K),
-// as bf16 hi/lo pairs.  Rows above 16 b are never read back.
+// rounded to tf32 (K-major fp32: thread c writes column c of every row, a
+// warp one 128-byte line).  Rows above 16 b are never read back.
 template <int B>
-__device__ __forceinline__ void build_version(const OperandLayout& XH, const OperandLayout& XL,
-                                              uint32_t tl, int c, const float (&p)[CH],
-                                              const float (&F)[4][4]) {
+__device__ __forceinline__ void build_version(const OperandLayout& XA, uint32_t tl, int c,
+                                              const float (&p)[CH], const float (&F)[4][4]) {
 #pragma unroll
   for (int a = B; a < 4; ++a) {
     float qv[16], kv[16];
@@ -197,17 +195,10 @@ __device__ __forceinline__ void build_version(const OperandLayout& XH, const Ope
     tmem_ld16(tl + TA_K + 16 * a, kv);
     tmem_ld_wait();
 #pragma unroll
-    for (int h8 = 0; h8 < 16; h8 += 8) {
-      float fq[8], fk[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float f = p[16 * a + h8 + j] * F[a][B];
-        fq[j] = qv[h8 + j] * f;
-        fk[j] = kv[h8 + j] * f;
-      }
-      const int r0 = 16 * a + h8;
-      st8_split(layout_addr(XH, r0, c), layout_addr(XL, r0, c), fq);
-      st8_split(layout_addr(XH, CH + r0, c), layout_addr(XL, CH + r0, c), fk);
+    for (int j = 0; j < 16; ++j) {
+      const float f = p[16 * a + j] * F[a][B];
+      st_f32(layout_addr(XA, 16 * a + j, c), tf32r(qv[j] * f));
+      st_f32(layout_addr(XA, CH + 16 * a + j, c), tf32r(kv[j] * f));
     }
   }
 }
@@ -507,10 +498,13 @@ __global__ void __launch_bounds__(128, 2)
     }
   }
 
-  // ---- M1: column tile b of [A_qk; A_kk], one tile version at a time
-  const OperandLayout XH = mnmajor(sb + A_XH, 16384), XL = mnmajor(sb + A_XL, 16384);
-  const OperandLayout KBH = mnmajor(sb + A_KBH, 16384), KBL = mnmajor(sb + A_KBL, 16384);
-  constexpr uint32_t ID_M1 = make_idesc(128, 16, true, true);
+  // ---- M1: column tile b of [A_qk; A_kk], one tile version at a time.
+  // kind::tf32 with fp32 operands: A = version b, [128 rows][128 channels];
+  // B = K-bar, [64 keys][128 channels]; both K-major.
+  OperandLayout XA = kmajor(sb + A_XH, 16384), KBA = kmajor(sb + A_KBH, 8192);
+  XA.esize = 4;
+  KBA.esize = 4;
+  constexpr uint32_t ID_M1 = make_idesc_tf32(128, 16, false, false);
   // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
   // M1 operands below overwrite
   if (tid == 0) bulk_wait_reads();
@@ -522,34 +516,23 @@ __global__ void __launch_bounds__(128, 2)
       tmem_ld16(tl + TA_K + 16 * a, kv);
       tmem_ld_wait();
 #pragma unroll
-      for (int h8 = 0; h8 < 16; h8 += 8) {
-        float fk[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) fk[j] = kv[h8 + j] * rcp(pr[16 * a + h8 + j]);
-        const int i0 = 16 * a + h8;
-        st8_split(layout_addr(KBH, i0, c), layout_addr(KBL, i0, c), fk);
-      }
+      for (int j = 0; j < 16; ++j)
+        st_f32(layout_addr(KBA, 16 * a + j, c), tf32r(kv[j] * rcp(pr[16 * a + j])));
     }
   }
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     if (!ok) break;
-    if (b == 0) build_version<0>(XH, XL, tl, c, pr, F);
-    if (b == 1) build_version<1>(XH, XL, tl, c, pr, F);
-    if (b == 2) build_version<2>(XH, XL, tl, c, pr, F);
-    if (b == 3) build_version<3>(XH, XL, tl, c, pr, F);
+    if (b == 0) build_version<0>(XA, tl, c, pr, F);
+    if (b == 1) build_version<1>(XA, tl, c, pr, F);
+    if (b == 2) build_version<2>(XA, tl, c, pr, F);
+    if (b == 3) build_version<3>(XA, tl, c, pr, F);
     operands_ready();
     if (tid == 0) {
       const uint32_t d = tmem + TA_A + 16 * b;
-      const uint64_t xh = layout_desc(XH, 0, 0), xl = layout_desc(XL, 0, 0);
-      const uint64_t bh = layout_desc(KBH, 16 * b, 0), bl = layout_desc(KBL, 16 * b, 0);
 #pragma unroll
-      for (int k0 = 0; k0 < DP; k0 += 16) {
-        const uint64_t ah = desc_adv(xh, k0, true), bhk = desc_adv(bh, k0, true);
-        umma_bf16(d, ah, bhk, ID_M1, k0 > 0);
-        umma_bf16(d, desc_adv(xl, k0, true), bhk, ID_M1, 1);
-        umma_bf16(d, ah, desc_adv(bl, k0, true), ID_M1, 1);
-      }
+      for (int k0 = 0; k0 < DP; k0 += 8)
+        umma_tf32(d, layout_desc(XA, 0, k0), layout_desc(KBA, 16 * b, k0), ID_M1, k0 > 0);
       umma_commit(bar_mma);
     }
     ok = wait_all(bar_mma, mma_phase);
