@@ -1080,11 +1080,11 @@ int segment_chunks(int nc_max) {
   return s < 32 ? 32 : (s + 15) / 16 * 16;
 }
 
-// The overlapped schedule pays off for long sequences and few states:
-// below 512 chunks its fill and drain cost more than the overlap gains, and
-// stage 2 must leave stage 1 at least half the SMs.
+// The overlapped schedule pays off for sequences of at least 128 chunks
+// (8192 tokens) and few states: stage 2 must leave stage 1 at least half
+// the SMs.
 bool use_overlap(int n_states, int nc_max, int sms) {
-  return n_states <= sms / 2 && nc_max >= 512;
+  return n_states <= sms / 2 && nc_max >= 128;
 }
 
 template <int DIN, typename OutT>
