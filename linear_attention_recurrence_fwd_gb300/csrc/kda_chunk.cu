@@ -95,6 +95,10 @@ constexpr uint32_t A_TI = 0;                              // T fp32 (in the W sl
 constexpr uint32_t A_DINV = 57344;                        // T_aa transposed, 4 KB (in the T diag(beta) slot, before it)
 constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
 constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
+// Stage 1 threads: thread t owns key channel (TMEM lane) t % 128 and, in the
+// per-token stages, the token tiles {0, 3} (t < 128) or {1, 2} (t >= 128);
+// that split gives both halves the same share of every M1 version build.
+constexpr int A_THREADS = 256;
 
 // ---- stage 2 shared memory
 constexpr uint32_t B_REC0 = 0, B_V0 = 66560, B_REC1 = 82944, B_V1 = 149504;
@@ -182,23 +186,41 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 __device__ __forceinline__ void set_status(int code) { atomicExch(&g_chunk_status, code); }
 
 // Version b of the M1 A operand: rows r >= 16 b of [Q^(b); K^(b)] with
-// Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r F[tile(r)][b] (same for K),
-// rounded to tf32 (K-major fp32: thread c writes column c of every row, a
-// warp one 128-byte line).  Rows above 16 b are never read back.
+// Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r e^{E_a - E_b} (a = tile of r; same
+// for K), rounded to tf32 (K-major fp32: a thread writes column c of every
+// row it owns, a warp one 128-byte line).  The calling thread builds the rows
+// of its two tiles ta[0], ta[1] (with p and Eo their p and tile ends).  Rows
+// above 16 b are never read back.
+// Address of element (row, channel c) of a K-major, 128-byte-swizzled fp32
+// operand: cbase = base + (c / 32) * kb_stride, cl = (c % 32) * 4.  Row
+// groups of 8 are 1024 bytes apart; the swizzle XORs the 16-byte chunk
+// index with row % 8.  For rows 16 a + j with j a compile-time constant the
+// row-dependent terms fold to constants.
+__device__ __forceinline__ uint32_t kmaj32_addr(uint32_t cbase, uint32_t cl, int row) {
+  return cbase + ((uint32_t)(row >> 3) << 10) + ((uint32_t)(row & 7) << 7) +
+         (cl ^ ((uint32_t)(row & 7) << 4));
+}
+
 template <int B>
-__device__ __forceinline__ void build_version(const OperandLayout& XA, uint32_t tl, int c,
-                                              const float (&p)[CH], const float (&F)[4][4]) {
+__device__ __forceinline__ void build_version(uint32_t xbase, uint32_t cl, uint32_t tl,
+                                              const float (&p)[2][16], const float (&Eo)[2],
+                                              float EB, const int (&ta)[2]) {
 #pragma unroll
-  for (int a = B; a < 4; ++a) {
+  for (int s = 0; s < 2; ++s) {
+    const int a = ta[s];
+    if (a < B) continue;  // warp-uniform
     float qv[16], kv[16];
     tmem_ld16(tl + TA_Q + 16 * a, qv);
     tmem_ld16(tl + TA_K + 16 * a, kv);
     tmem_ld_wait();
+    const float fab = ex2((Eo[s] - EB) * LOG2E);  // e^{E_a - E_b} in [e^-240, 1]
+    const uint32_t qrow = xbase + ((uint32_t)a << 11);  // rows 16 a .. 16 a + 15
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float f = p[16 * a + j] * F[a][B];
-      st_f32(layout_addr(XA, 16 * a + j, c), tf32r(qv[j] * f));
-      st_f32(layout_addr(XA, CH + 16 * a + j, c), tf32r(kv[j] * f));
+      const float f = p[s][j] * fab;
+      const uint32_t at = kmaj32_addr(qrow, cl, j);
+      st_f32(at, tf32r(qv[j] * f));
+      st_f32(at + (CH / 8) * 1024, tf32r(kv[j] * f));  // row CH + 16 a + j
     }
   }
 }
@@ -216,7 +238,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
                                             int tid) {
   constexpr int kStrips = (4 - S) * 64;  // (block, row, 4-column quad)
 #pragma unroll
-  for (int st = tid; st < kStrips; st += 128) {
+  for (int st = tid; st < kStrips; st += A_THREADS) {
     const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
@@ -237,7 +259,7 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
   }
   __syncthreads();
 #pragma unroll
-  for (int st = tid; st < kStrips; st += 128) {
+  for (int st = tid; st < kStrips; st += A_THREADS) {
     const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
@@ -266,15 +288,15 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
 // which is free once M1 is done; one thread per position pair walks the
 // channels starting at a thread-dependent offset so a warp's loads fall in
 // distinct banks.  res[0..1023] receives A_qk and res[1024..2047] A_kk, as
-// [tile][r % 16][i % 16].  Called by all 128 threads of the CTA.
+// [tile][r % 16][i % 16].  Called by all threads of the CTA.
 __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
                                                      float* res) {
   uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
   uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
   float* sg = reinterpret_cast<float*>(sbp + 32768);
-  const int c = tid;
+  const int c = tid & (DP - 1), t_lo = (tid >> 7) * 32;  // this thread: channel c, 32 tokens
 #pragma unroll 1
-  for (int t0 = 0; t0 < CH; t0 += 16) {
+  for (int t0 = t_lo; t0 < t_lo + 32; t0 += 16) {
     float qv[16], kv[16], gv[16];
     tmem_ld16(tl + TA_Q + t0, qv);
     tmem_ld16(tl + TA_K + t0, kv);
@@ -289,7 +311,7 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
   }
   __syncthreads();
 #pragma unroll 1
-  for (int pidx = tid; pidx < 4 * 136; pidx += 128) {
+  for (int pidx = tid; pidx < 4 * 136; pidx += A_THREADS) {
     const int a = pidx / 136, idx = pidx - 136 * a;
     int rr = 0;
     while ((rr + 1) * (rr + 2) / 2 <= idx) ++rr;
@@ -324,13 +346,15 @@ struct IntraParams {
 };
 
 template <int DIN, bool PAIRS>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(A_THREADS, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
   // One CTA per item (chunk, head), two CTAs per SM.  The item loop also
   // covers a grid smaller than the work list.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int c = tid & (DP - 1), hh = tid >> 7;  // key channel (TMEM lane); token half
+  const int ta[2] = {hh ? 1 : 0, hh ? 2 : 3};   // the token tiles this thread owns
   const int H = p.H;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -356,7 +380,7 @@ __global__ void __launch_bounds__(128, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_s;
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   uint32_t tma_phase = 0, mma_phase = 0;
   bool ok = true;
 
@@ -423,7 +447,7 @@ __global__ void __launch_bounds__(128, 2)
   const float beta_t = tid < valid ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
   __syncthreads();
   if (DIN == 64) {  // upper channel half of the raw tiles stays zero
-    for (uint32_t off = tid * 16; off < 8192; off += 128 * 16) {
+    for (uint32_t off = tid * 16; off < 8192; off += A_THREADS * 16) {
       st_shared_v4(sb + A_RQ + 8192 + off, 0, 0, 0, 0);
       st_shared_v4(sb + A_RK + 8192 + off, 0, 0, 0, 0);
       st_shared_v4(sb + A_RG + 8192 + off, 0, 0, 0, 0);
@@ -432,9 +456,9 @@ __global__ void __launch_bounds__(128, 2)
   // L[r][i] = (i <= r), I[r][i] = (i == r), both restricted to valid tokens i
   const OperandLayout LM = kmajor(sb + A_LM, 0), IM = kmajor(sb + A_IM, 0);
   {
-    const int r = tid >> 1, i_lo = (tid & 1) * 32;
+    const int r = tid >> 2, i_lo = (tid & 3) * 16;
 #pragma unroll
-    for (int i0 = i_lo; i0 < i_lo + 32; i0 += 8) {
+    for (int i0 = i_lo; i0 < i_lo + 16; i0 += 8) {
       float l[8], e[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -453,11 +477,10 @@ __global__ void __launch_bounds__(128, 2)
   tc_fence_after_sync();
 
   ok = wait_all(bar_tma, tma_phase);
-  const int c = tid;  // key channel owned in the elementwise stages
   if (ok && p.check_decay) {
     bool bad = false;
     const OperandLayout RG = kmajor(sb + A_RG, 8192);
-    for (int i = 0; i < valid; ++i) {
+    for (int i = 32 * hh; i < valid && i < 32 * hh + 32; ++i) {
       const float la = bf2f(ld_shared_u16(layout_addr(RG, i, c)));
       bad |= !(la >= -5.f && la <= 0.f);
     }
@@ -480,21 +503,22 @@ __global__ void __launch_bounds__(128, 2)
   }
   if (ok) ok = wait_all(bar_mma, mma_phase);
 
-  // ---- per-channel decay factors (thread = channel c, TMEM lane c)
-  float pr[CH], F[4][4], GE[4];
+  // ---- decay factors of this thread's channel and tiles: E[b] = g at the
+  // end of tile b; p[s][j] = e^{g - E} of token 16 ta[s] + j, in [1, e^80]
+  float E[4], Eo[2], pr[2][16];
   if (ok) {
-    float g[CH];
-    tmem_ld64(tl + TA_G, g);
-    float E[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) E[b] = g[16 * b + 15];
+    for (int b = 0; b < 4; ++b) E[b] = tmem_ld1(tl + TA_G + 16 * b + 15);
+    float g0[16], g1[16];
+    tmem_ld16(tl + TA_G + 16 * ta[0], g0);
+    tmem_ld16(tl + TA_G + 16 * ta[1], g1);
+    tmem_ld_wait();
+    Eo[0] = hh ? E[1] : E[0];
+    Eo[1] = hh ? E[2] : E[3];
 #pragma unroll
-    for (int i = 0; i < CH; ++i) pr[i] = ex2((g[i] - E[i / 16]) * LOG2E);  // [1, e^80]
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      GE[a] = ex2(E[a] * LOG2E);
-#pragma unroll
-      for (int b = 0; b < 4; ++b) F[a][b] = a > b ? ex2((E[a] - E[b]) * LOG2E) : 1.f;
+    for (int j = 0; j < 16; ++j) {
+      pr[0][j] = ex2((g0[j] - Eo[0]) * LOG2E);
+      pr[1][j] = ex2((g1[j] - Eo[1]) * LOG2E);
     }
   }
 
@@ -509,24 +533,28 @@ __global__ void __launch_bounds__(128, 2)
   // M1 operands below overwrite
   if (tid == 0) bulk_wait_reads();
   __syncthreads();
-  if (ok) {
+  const uint32_t cl = (uint32_t)(c & 31) * 4;
+  const uint32_t xbase = sb + A_XH + (uint32_t)(c >> 5) * 16384;
+  if (ok) {  // K-bar = k e^{E - g} for this thread's tiles
+    const uint32_t kbase = sb + A_KBH + (uint32_t)(c >> 5) * 8192;
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int s2 = 0; s2 < 2; ++s2) {
       float kv[16];
-      tmem_ld16(tl + TA_K + 16 * a, kv);
+      tmem_ld16(tl + TA_K + 16 * ta[s2], kv);
       tmem_ld_wait();
+      const uint32_t krow = kbase + ((uint32_t)ta[s2] << 11);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        st_f32(layout_addr(KBA, 16 * a + j, c), tf32r(kv[j] * rcp(pr[16 * a + j])));
+        st_f32(kmaj32_addr(krow, cl, j), tf32r(kv[j] * rcp(pr[s2][j])));
     }
   }
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     if (!ok) break;
-    if (b == 0) build_version<0>(XA, tl, c, pr, F);
-    if (b == 1) build_version<1>(XA, tl, c, pr, F);
-    if (b == 2) build_version<2>(XA, tl, c, pr, F);
-    if (b == 3) build_version<3>(XA, tl, c, pr, F);
+    if (b == 0) build_version<0>(xbase, cl, tl, pr, Eo, E[0], ta);
+    if (b == 1) build_version<1>(xbase, cl, tl, pr, Eo, E[1], ta);
+    if (b == 2) build_version<2>(xbase, cl, tl, pr, Eo, E[2], ta);
+    if (b == 3) build_version<3>(xbase, cl, tl, pr, Eo, E[3], ta);
     operands_ready();
     if (tid == 0) {
       const uint32_t d = tmem + TA_A + 16 * b;
@@ -551,51 +579,67 @@ __global__ void __launch_bounds__(128, 2)
   const OperandLayout TB = kmajor(sb + A_STG + REC_TB, 0);
   const OperandLayout WT = mnmajor(sb + A_WST, 16384);
   if (ok) {
-    // ---- A_qk (fp16 record image) and beta-scaled strictly-lower A_kk (fp32)
+    // ---- A_qk (fp16 record image) and beta-scaled strictly-lower A_kk (fp32):
+    // TMEM lane c is row c of [A_qk; A_kk]; this thread takes columns
+    // [32 hh, 32 hh + 32).
     {
-      float a[64];
-      tmem_ld64(tl + TA_A, a);
-      if (PAIRS) {  // this row's diagonal tile from the per-pair path
-        const int m = tid < CH ? tid : tid - CH;
-        const float* row = s_pair + (tid < CH ? 0 : 1024) + (m >> 4) * 256 + (m & 15) * 16;
+      const int i_lo = 32 * hh;
+      float a0[16], a1[16];
+      tmem_ld16(tl + TA_A + i_lo, a0);
+      tmem_ld16(tl + TA_A + i_lo + 16, a1);
+      tmem_ld_wait();
+      float a[32];
 #pragma unroll
-        for (int i = 0; i < CH; ++i)
-          if ((i >> 4) == (m >> 4) && (i & 15) <= (m & 15)) a[i] = row[i & 15];
+      for (int j = 0; j < 16; ++j) {
+        a[j] = a0[j];
+        a[16 + j] = a1[j];
       }
-      if (warp < 2) {
-        const int r = tid;
+      const int r = c < CH ? c : c - CH;
+      if (PAIRS && ((r >> 5) == hh)) {  // this row's diagonal tile from the per-pair path
+        const float* row = s_pair + (c < CH ? 0 : 1024) + (r >> 4) * 256 + (r & 15) * 16;
+        const int o = 16 * ((r >> 4) & 1);  // offset of the diagonal tile in a[]
 #pragma unroll
-        for (int i0 = 0; i0 < CH; i0 += 8) {
+        for (int jj = 0; jj < 16; ++jj)
+          if (jj <= (r & 15)) {
+            if (o == 0) a[jj] = row[jj]; else a[16 + jj] = row[jj];
+          }
+      }
+      if (c < CH) {
+#pragma unroll
+        for (int i0 = 0; i0 < 32; i0 += 8) {
           float x[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = (i0 + j <= r) ? a[i0 + j] : 0.f;
-          st8h(layout_addr(AQ, r, i0), x);
+          for (int j = 0; j < 8; ++j) x[j] = (i_lo + i0 + j <= r) ? a[i0 + j] : 0.f;
+          st8h(layout_addr(AQ, r, i_lo + i0), x);
         }
       } else {  // stored transposed, akk[i][r] = L[r][i]: the solve reads L by columns
-        const int r = tid - CH;
         const float br = s_beta[r];
 #pragma unroll
-        for (int i = 0; i < CH; ++i) akk[i * CH + r] = (i < r) ? br * a[i] : 0.f;
+        for (int i = 0; i < 32; ++i) akk[(i_lo + i) * CH + r] = (i_lo + i < r) ? br * a[i] : 0.f;
       }
     }
     if (PAIRS) __syncthreads();  // s_pair is overwritten by (k e^g)^T below
-    // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record images)
+    // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record
+    // images), for this thread's channel and tiles
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const int a = ta[s2];
       float qv[16], kv[16];
       tmem_ld16(tl + TA_Q + 16 * a, qv);
       tmem_ld16(tl + TA_K + 16 * a, kv);
       tmem_ld_wait();
+      const float ge = ex2(Eo[s2] * LOG2E);             // e^{E_a}
+      const float f3 = ex2((E[3] - Eo[s2]) * LOG2E);   // e^{E_3 - E_a}
 #pragma unroll
       for (int h8 = 0; h8 < 16; h8 += 8) {
         float kt[8], qt[8], kb[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int i = 16 * a + h8 + j;
-          const float gam = pr[i] * GE[a];  // e^{g_i}
+          const float pj = pr[s2][h8 + j];
+          const float gam = pj * ge;  // e^{g_i}
           kt[j] = kv[h8 + j] * gam;
           qt[j] = qv[h8 + j] * gam;
-          kb[j] = kv[h8 + j] * rcp(pr[i]) * F[3][a];  // e^{g_C - g_i}
+          kb[j] = kv[h8 + j] * rcp(pj) * f3;  // e^{g_C - g_i}
         }
         const int i0 = 16 * a + h8;
         st8(layout_addr(KT, c, i0), kt);
@@ -603,7 +647,7 @@ __global__ void __launch_bounds__(128, 2)
         st8h(layout_addr(KBAR, c, i0), kb);
       }
     }
-    s_gamma[c] = GE[3];
+    if (hh == 0) s_gamma[c] = ex2(E[3] * LOG2E);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
@@ -641,9 +685,9 @@ __global__ void __launch_bounds__(128, 2)
     solve_level<3>(akk, ti, dinv, tid);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
-      const int r = tid >> 1, i_lo = (tid & 1) * 32;
+      const int r = tid >> 2, i_lo = (tid & 3) * 16;
 #pragma unroll
-      for (int i0 = i_lo; i0 < i_lo + 32; i0 += 8) {
+      for (int i0 = i_lo; i0 < i_lo + 16; i0 += 8) {
         const float4 t0 = *reinterpret_cast<const float4*>(ti + tix(r, i0));
         const float4 t1 = *reinterpret_cast<const float4*>(ti + tix(r, i0 + 4));
         const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
@@ -669,10 +713,14 @@ __global__ void __launch_bounds__(128, 2)
   }
   if (ok) {
     // ---- W (fp16, N = r, K = c) from W^T in TMEM (lane = c), into the (k e^g)^T slot
-    float w[64];
-    tmem_ld64(tl + TA_W, w);
-#pragma unroll
-    for (int r0 = 0; r0 < CH; r0 += 8) st8h(layout_addr(WT, r0, c), w + r0);
+    float w0[16], w1[16];
+    tmem_ld16(tl + TA_W + 32 * hh, w0);
+    tmem_ld16(tl + TA_W + 32 * hh + 16, w1);
+    tmem_ld_wait();
+    st8h(layout_addr(WT, 32 * hh, c), w0);
+    st8h(layout_addr(WT, 32 * hh + 8, c), w0 + 8);
+    st8h(layout_addr(WT, 32 * hh + 16, c), w1);
+    st8h(layout_addr(WT, 32 * hh + 24, c), w1 + 8);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -1112,7 +1160,7 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
                    dependent ? grid_done : nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)items);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(A_THREADS);
     cfg.dynamicSmemBytes = A_SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
