@@ -926,17 +926,19 @@ __global__ void __launch_bounds__(B_THREADS, 1)
           const uint64_t dut = layout_desc(UT, 0, 0);
           const uint64_t daq = layout_desc(kmajor(rb + REC_AQ, 0), 0, 0);
           const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
+          // M6 first: the chain waits only for the state update; the second
+          // half of M5 (the output) runs while the chain rebuilds S^T
 #pragma unroll
-          for (int k0 = 0; k0 < CH; k0 += 16) {
-            const uint64_t a = desc_adv(dut, k0, false);
-            umma_bf16(tmem + TB_S, a, desc_adv(dkb, k0, false), ID_S, 1);  // M6
-            umma_bf16(td + 64, a, desc_adv(daq, k0, false), ID_O2, 1);    // M5, second half
-          }
+          for (int k0 = 0; k0 < CH; k0 += 16)
+            umma_bf16(tmem + TB_S, desc_adv(dut, k0, false), desc_adv(dkb, k0, false), ID_S, 1);
           umma_commit(mma_b);
+#pragma unroll
+          for (int k0 = 0; k0 < CH; k0 += 16)
+            umma_bf16(td + 64, desc_adv(dut, k0, false), desc_adv(daq, k0, false), ID_O2, 1);
           umma_commit(&o_full[ob]);
         }
         if (j + 2 < nchunks) {  // buffer buf is consumed once every product of chunk j is done
-          if (!(ok = mbar_wait(mma_b, j & 1))) break;
+          if (!(ok = mbar_wait(&o_full[ob], (j >> 1) & 1))) break;
           fence_proxy_async_smem();
           issue_loads(j + 2, buf);
           ++issued;
