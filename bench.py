@@ -234,7 +234,18 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
     res["ablation_diag_per_pair"] = {
         "workload": "prefill_64k with the diagonal tiles evaluated per position pair",
         "ms": ms, "Mtok_s": ws * tok / ms / 1e3, "slowdown_vs_dense": ms / ms64, "steps": 5}
-    del out, fin, a64
+    # the same problem saving the state every 512 tokens (a prefix cache)
+    ck = torch.empty((1, x64["q"].shape[1] // 512, x64["q"].shape[2], 128, 128),
+                     dtype=torch.float32, device=dev)
+    ms_ck = reduce_max(time_call(lambda: binding.kda_chunk_fwd_checkpointed(
+        *a64, x64["initial_state"], checkpoint_every=512, out=out, final_state=fin,
+        checkpoints=ck), 10, 3, stream), ws)
+    res["prefill_64k_checkpoints_512"] = {
+        "workload": "prefill_64k, state saved every 512 tokens "
+                    f"({ck.shape[1]} x {ck.shape[2]} heads x 64 KiB)",
+        "ms": ms_ck, "Mtok_s": ws * tok / ms_ck / 1e3, "overhead_vs_plain": ms_ck / ms64 - 1,
+        "steps": 10}
+    del out, fin, a64, ck
 
     def fixed(name, steps):
         w = gen.WORKLOADS[name]

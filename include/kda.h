@@ -107,6 +107,31 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
  * B * ceil(T / 64) * H * 66560 + B * H * 65536 + 256. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
+/*
+ * kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also saves the recurrent
+ * state at fixed token boundaries, for a prefix cache.  The orkas.ai page
+ * ("Kimi K3 architecture", section "Die Rechnung landet in der
+ * Bereitstellungsinfrastruktur") describes hashing prefixes every 512
+ * tokens and keeping the fixed-size recurrent state only at a sparse subset
+ * of those boundaries; this call writes it at every checkpoint_every tokens.
+ *   checkpoint_every : tokens between checkpoints, a positive multiple of 64
+ *                      (KDA_ERR_INVALID_ARG otherwise)
+ *   checkpoints      : [B, T / checkpoint_every, H, d_k, d_v] fp32 (16-byte
+ *                      aligned; may be NULL when T < checkpoint_every).
+ *                      Entry [b, n] is the state after the first
+ *                      (n + 1) * checkpoint_every tokens of sequence b.
+ * Every other argument, the workspace size and the results are those of
+ * kda_chunk_fwd.
+ */
+KDA_API kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void* v,
+                                                const void* log_alpha, const void* beta,
+                                                const float* initial_state, void* out,
+                                                kda_dtype_t out_dtype, float* final_state,
+                                                int B, int T, int H, int d_k, int d_v,
+                                                float scale, float* checkpoints,
+                                                int checkpoint_every, void* workspace,
+                                                size_t workspace_bytes, cudaStream_t stream);
+
 /* Kernel launches one kda_chunk_fwd call of this shape makes on the current
  * device (the schedule depends on the device's SM count): 2 for the plain
  * two-stage schedule, 2 per segment for the overlapped one.  -1 on a bad

@@ -24,7 +24,7 @@ STATUS = {
 }
 
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
-           "kda_chunk_fwd_launches",
+           "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches",
            "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
            "kda_last_device_status", "kda_version"]
@@ -53,6 +53,9 @@ def load(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         lib.kda_chunk_fwd.argtypes = [_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
         lib.kda_chunk_fwd.restype = _i
+        lib.kda_chunk_fwd_checkpointed.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f] +
+                                                   [_vp, _i, _vp, _sz, _vp])
+        lib.kda_chunk_fwd_checkpointed.restype = _i
         lib.kda_chunk_fwd_noalloc.argtypes = [_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _vp]
         lib.kda_chunk_fwd_noalloc.restype = _i
         lib.kda_varlen_fwd.argtypes = [_vp] * 6 + [_i, _i, _i, _vp, _vp, _i, _vp, _i, _i, _i, _f,
@@ -140,6 +143,35 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
                              _p(out), _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv,
                              float(scale), _p(ws), ws_bytes, _stream(stream)), "kda_chunk_fwd")
     return out, final_state
+
+
+def kda_chunk_fwd_checkpointed(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
+                               checkpoint_every=512, out_dtype=torch.float32, out=None,
+                               final_state=None, checkpoints=None, stream=None):
+    """kda_chunk_fwd plus the state after every `checkpoint_every` tokens.
+    Returns (out, final_state, checkpoints [B, T // checkpoint_every, H, dk, dv])."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    if initial_state is not None:
+        _need(initial_state, torch.float32, "initial_state")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    n_ckpt = T // checkpoint_every if checkpoint_every > 0 else 0
+    if checkpoints is None:
+        checkpoints = torch.empty((B, n_ckpt, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws_bytes = lib.kda_chunk_fwd_workspace_size(B, T, H, dk, dv)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    _check(lib.kda_chunk_fwd_checkpointed(
+        _p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state), _p(out),
+        _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv, float(scale),
+        _p(checkpoints) if n_ckpt else None, int(checkpoint_every), _p(ws), ws_bytes,
+        _stream(stream)), "kda_chunk_fwd_checkpointed")
+    return out, final_state, checkpoints
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,

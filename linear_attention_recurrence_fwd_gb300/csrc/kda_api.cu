@@ -105,6 +105,32 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
+kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void* v,
+                                        const void* log_alpha, const void* beta,
+                                        const float* initial_state, void* out,
+                                        kda_dtype_t out_dtype, float* final_state, int B, int T,
+                                        int H, int d_k, int d_v, float scale, float* checkpoints,
+                                        int checkpoint_every, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || T < 0 || checkpoint_every <= 0 || checkpoint_every % 64) return KDA_ERR_INVALID_ARG;
+  const int n_ckpt = T / checkpoint_every;
+  if (n_ckpt > 0 && !checkpoints) return KDA_ERR_INVALID_ARG;
+  if (n_ckpt > 0 && !aligned16(checkpoints)) return KDA_ERR_ALIGNMENT;
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
+                                     final_state, H, d_k, d_v, (long long)B * T > 0);
+  if (st != KDA_OK) return st;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  const size_t need = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v);
+  if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(),
+                      ablate_diag_env(), n_ckpt > 0 ? checkpoints : nullptr,
+                      checkpoint_every / 64, n_ckpt};
+  return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
+}
+
 kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
                                    const void* log_alpha, const void* beta,
                                    const float* initial_state, void* out, kda_dtype_t out_dtype,

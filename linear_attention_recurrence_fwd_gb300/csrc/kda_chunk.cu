@@ -762,6 +762,8 @@ struct StateParams {
   int T, n_seq, H;
   int j_lo, j_hi;
   float scale;
+  float* ckpt;  // state after every ckpt_every chunks ([n_seq][n_ckpt][H][d][d]), or null
+  int ckpt_every, n_ckpt;
 };
 
 // Stage 2 warp roles: warps 0-7 run the elementwise part of the serial
@@ -1046,6 +1048,13 @@ __global__ void __launch_bounds__(B_THREADS, 1)
           for (int c0 = 0; c0 < 64; ++c0)
             if (c_lo + c0 < DIN) s_out[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
         }
+        const int done = jb + j + 1;  // chunks of the sequence finished
+        if (p.ckpt && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.n_ckpt && v < DIN) {
+          float* ck = p.ckpt + ((size_t)(n * p.n_ckpt + done / p.ckpt_every - 1) * H + h) * DIN * DIN;
+#pragma unroll
+          for (int c0 = 0; c0 < 64; ++c0)
+            if (c_lo + c0 < DIN) ck[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+        }
       }
     }
     if (!ok) fail();
@@ -1175,7 +1184,8 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   };
   auto state = [&](int j_lo, int j_hi) -> cudaError_t {
     StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, pr.cu_seqlens,
-                   chunk_base, pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale};
+                   chunk_base, pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale,
+                   pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt};
     kda_state_kernel<DIN, OutT>
         <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
     return cudaGetLastError();

@@ -31,6 +31,10 @@ struct ChunkProblem {
   float scale;
   bool check_decay;
   bool diag_per_pair;  // ablation: diagonal tiles per position pair on CUDA cores
+  // state checkpoints (fixed-length only): after every ckpt_every_chunks
+  // chunks of a sequence, n_ckpt of them, [n_seq][n_ckpt][H][d][d]
+  float* ckpt;
+  int ckpt_every_chunks, n_ckpt;
 };
 
 // Device workspace the chunked prefill needs: per-(chunk, head) records

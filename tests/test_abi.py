@@ -99,3 +99,14 @@ def test_chunk_workspace_is_required_and_sized(lib):
                              F, need - 16, None) == 7
     vneed = lib.kda_varlen_fwd_workspace_size(4, 1000, 2, 128, 128)
     assert vneed == 1024 + (1000 // 64 + 4) * 2 * 66560 + 4 * 2 * 65536 + 256
+
+
+def test_checkpointed_argument_errors(lib):
+    def call(every=512, ck=F, T=1024, ws=None, wsb=0):
+        return lib.kda_chunk_fwd_checkpointed(F, F, F, F, F, None, F, 0, None, 1, T, 2, 128, 128,
+                                              1.0, ck, every, ws, wsb, None)
+    assert call(every=0) == 1             # not positive
+    assert call(every=100) == 1           # not a multiple of 64
+    assert call(ck=None) == 1             # checkpoints needed: T >= checkpoint_every
+    assert call(ck=ctypes.c_void_p(24)) == 3
+    assert call() == 7                    # valid, but no workspace
