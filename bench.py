@@ -261,6 +261,27 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
 
     fixed("prefill_8k", 20)
 
+    # speculative decoding: verify 4 drafted tokens per sequence (state read
+    # once), then commit all 4 (state read and written once)
+    wd = gen.WORKLOADS["decode"]
+    K = 4
+    xd = gen.make_inputs(wd.B, K, wd.H, 128, 128, wd.seed, init_std=wd.init_std, device=dev)
+    dd = [xd[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    st = xd["initial_state"]
+    vo = torch.empty((wd.B, K, wd.H, 128), dtype=torch.float32, device=dev)
+    acc = torch.full((wd.B,), K, dtype=torch.int32, device=dev)
+    ms_v = reduce_max(time_call(lambda: binding.kda_decode_verify(*dd, st, out=vo), 50, 3,
+                                stream), ws)
+    ms_c = reduce_max(time_call(lambda: binding.kda_decode_commit(*dd, st, acc), 50, 3, stream),
+                      ws)
+    sbytes = wd.B * wd.H * 128 * 128 * 4
+    io = wd.B * K * wd.H * (4 * 128 * 2 + 2)
+    res["speculative_verify_commit_k4"] = {
+        "workload": f"{wd.B} seq x {wd.H} heads, {K} drafted tokens",
+        "verify_us": ms_v * 1e3, "verify_gbs": (sbytes + io + wd.B * K * wd.H * 128 * 4) / ms_v / 1e6,
+        "commit_us": ms_c * 1e3, "commit_gbs": (2 * sbytes + io) / ms_c / 1e6, "steps": 50}
+    del xd, dd, st, vo
+
     w = gen.WORKLOADS["varlen_64k"]
     x = gen.workload_inputs(w, device=dev)
     cu = gen.cu_seqlens_of(w.seqlens).to(dev)

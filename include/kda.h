@@ -211,6 +211,36 @@ KDA_API kda_status_t kda_decode_step(const void* q, const void* k, const void* v
                              int N, int H, int d_k, int d_v, float scale,
                              cudaStream_t stream);
 
+/*
+ * Speculative decoding.  The state is updated in place, so a rejected draft
+ * cannot be undone; instead the draft's projected inputs (much smaller than
+ * the state) are kept and the state is rebuilt on chip from them (orkas.ai,
+ * "Kimi K3 architecture", section "Die Rechnung landet in der
+ * Bereitstellungsinfrastruktur").  Each call reads the state once.
+ *
+ * kda_decode_verify -- outputs of K drafted tokens per sequence, the
+ * recurrence applied token after token from `state`, which is only read.
+ *   q, k, log_alpha : [N, K, H, d_k] bf16;  v : [N, K, H, d_v] bf16
+ *   beta            : [N, K, H] bf16;      state : [N, H, d_k, d_v] fp32
+ *   out             : [N, K, H, d_v] in out_dtype; token t of sequence n is
+ *                     the output kda_decode_step would give after tokens
+ *                     0..t of the draft.
+ * kda_decode_commit -- advance each sequence's state, in place, by the first
+ * accepted[n] tokens of the same draft inputs (accepted: DEVICE int32 [N],
+ * clamped to [0, K]); the state afterwards equals that of accepted[n]
+ * kda_decode_step calls.
+ * Supported head dims: d_k = d_v = 128.
+ */
+KDA_API kda_status_t kda_decode_verify(const void* q, const void* k, const void* v,
+                                       const void* log_alpha, const void* beta,
+                                       const float* state, void* out, kda_dtype_t out_dtype,
+                                       int N, int K, int H, int d_k, int d_v, float scale,
+                                       cudaStream_t stream);
+KDA_API kda_status_t kda_decode_commit(const void* q, const void* k, const void* v,
+                                       const void* log_alpha, const void* beta, float* state,
+                                       const int* accepted, int N, int K, int H, int d_k,
+                                       int d_v, cudaStream_t stream);
+
 /* Static description of a status code (never NULL). */
 KDA_API const char* kda_status_string(kda_status_t status);
 

@@ -24,7 +24,8 @@ STATUS = {
 }
 
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
-           "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches",
+           "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches", "kda_decode_verify",
+           "kda_decode_commit",
            "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
            "kda_last_device_status", "kda_version"]
@@ -63,6 +64,10 @@ def load(path: str = LIB_PATH):
         lib.kda_varlen_fwd.restype = _i
         lib.kda_decode_step.argtypes = [_vp] * 7 + [_i, _i, _i, _i, _i, _f, _vp]
         lib.kda_decode_step.restype = _i
+        lib.kda_decode_verify.argtypes = [_vp] * 7 + [_i, _i, _i, _i, _i, _i, _f, _vp]
+        lib.kda_decode_verify.restype = _i
+        lib.kda_decode_commit.argtypes = [_vp] * 7 + [_i, _i, _i, _i, _i, _vp]
+        lib.kda_decode_commit.restype = _i
         lib.kda_chunk_fwd_workspace_size.argtypes = [_i] * 5
         lib.kda_chunk_fwd_workspace_size.restype = _sz
         lib.kda_varlen_fwd_workspace_size.argtypes = [_i] * 5
@@ -236,6 +241,41 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, scale=1.0, out=None,
                                _dtype_code(out.dtype), N, H, dk, dv, float(scale),
                                _stream(stream)), "kda_decode_step")
     return out
+
+
+def kda_decode_verify(q, k, v, log_alpha, beta, state, scale=1.0, out_dtype=torch.float32,
+                      out=None, stream=None):
+    """Outputs of K drafted tokens per sequence from `state` (only read).
+    q, k, log_alpha, v [N,K,H,d] bf16; beta [N,K,H]; state [N,H,d,d] fp32.
+    Returns out [N,K,H,d]."""
+    lib = load()
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    _need(state, torch.float32, "state")
+    if out is None:
+        out = torch.empty((N, K, H, dv), dtype=out_dtype, device=q.device)
+    _check(lib.kda_decode_verify(_p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(state),
+                                 _p(out), _dtype_code(out.dtype), N, K, H, dk, dv, float(scale),
+                                 _stream(stream)), "kda_decode_verify")
+    return out
+
+
+def kda_decode_commit(q, k, v, log_alpha, beta, state, accepted, stream=None):
+    """Advance `state` in place by the first accepted[n] draft tokens of each
+    sequence (accepted: int32 [N] on the device)."""
+    lib = load()
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    _need(state, torch.float32, "state")
+    _need(accepted, torch.int32, "accepted")
+    _check(lib.kda_decode_commit(_p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(state),
+                                 _p(accepted), N, K, H, dk, dv, _stream(stream)),
+           "kda_decode_commit")
+    return state
 
 
 def kda_chunk_fwd_launches(B, T, H):

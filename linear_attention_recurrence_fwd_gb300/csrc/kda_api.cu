@@ -195,6 +195,48 @@ int kda_chunk_fwd_launches(int B, int T, int H) {
   return kda::chunk_fwd_launches(false, B, T, H);
 }
 
+namespace {
+kda_status_t validate_multi(const void* q, const void* k, const void* v, const void* log_alpha,
+                            const void* beta, const void* state, int N, int K, int H, int d_k,
+                            int d_v) {
+  if (N < 0 || K < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if ((long long)N * K > 0 && (!q || !k || !v || !log_alpha || !beta || !state))
+    return KDA_ERR_INVALID_ARG;
+  if (d_k != 128 || d_v != 128) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+      !aligned2(beta) || !aligned16(state))
+    return KDA_ERR_ALIGNMENT;
+  if ((long long)N * H > 0x3fffffffLL || (long long)N * K * H > 0x7fffffffLL)
+    return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+}  // namespace
+
+kda_status_t kda_decode_verify(const void* q, const void* k, const void* v, const void* log_alpha,
+                               const void* beta, const float* state, void* out,
+                               kda_dtype_t out_dtype, int N, int K, int H, int d_k, int d_v,
+                               float scale, cudaStream_t stream) {
+  kda_status_t st = validate_multi(q, k, v, log_alpha, beta, state, N, K, H, d_k, d_v);
+  if (st != KDA_OK) return st;
+  if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if ((long long)N * K > 0 && (!out || !aligned16(out))) return out ? KDA_ERR_ALIGNMENT : KDA_ERR_INVALID_ARG;
+  if ((long long)N * K == 0) return KDA_OK;
+  return from_cuda(kda::launch_decode_tokens(q, k, v, log_alpha, beta, state, nullptr, out,
+                                             out_dtype == KDA_F32, nullptr, N, K, H, scale,
+                                             stream));
+}
+
+kda_status_t kda_decode_commit(const void* q, const void* k, const void* v, const void* log_alpha,
+                               const void* beta, float* state, const int* accepted, int N, int K,
+                               int H, int d_k, int d_v, cudaStream_t stream) {
+  kda_status_t st = validate_multi(q, k, v, log_alpha, beta, state, N, K, H, d_k, d_v);
+  if (st != KDA_OK) return st;
+  if (N > 0 && !accepted) return KDA_ERR_INVALID_ARG;
+  if ((long long)N * K == 0) return KDA_OK;
+  return from_cuda(kda::launch_decode_tokens(q, k, v, log_alpha, beta, state, state, nullptr,
+                                             true, accepted, N, K, H, 1.f, stream));
+}
+
 kda_status_t kda_last_device_status(cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   const int s = kda::read_and_clear_chunk_status(stream, &e);

@@ -14,6 +14,12 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
                                const void* log_alpha, const void* beta, float* state, void* out,
                                bool out_f32, int N, int H, float scale, cudaStream_t stream);
 
+// K tokens per (sequence, head) from one read of the state (see kda_decode.cu).
+cudaError_t launch_decode_tokens(const void* q, const void* k, const void* v,
+                                 const void* log_alpha, const void* beta, const float* state_in,
+                                 float* state_out, void* out, bool out_f32, const int* counts,
+                                 int N, int K, int H, float scale, cudaStream_t stream);
+
 // Chunked prefill over either B fixed-length sequences (cu_seqlens == null,
 // every sequence T tokens, tensors [B,T,H,d]) or N packed sequences
 // (cu_seqlens on the device, tensors [T_total,H,d]).

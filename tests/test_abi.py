@@ -110,3 +110,15 @@ def test_checkpointed_argument_errors(lib):
     assert call(ck=None) == 1             # checkpoints needed: T >= checkpoint_every
     assert call(ck=ctypes.c_void_p(24)) == 3
     assert call() == 7                    # valid, but no workspace
+
+
+def test_speculative_argument_errors(lib):
+    v = lambda N=2, K=3, dk=128, st=F, out=F: lib.kda_decode_verify(
+        F, F, F, F, F, st, out, 1, N, K, 2, dk, 128, 1.0, None)
+    assert v(N=-1) == 1
+    assert v(dk=64) == 2
+    assert v(st=ctypes.c_void_p(24)) == 3
+    assert v(out=None) == 1
+    assert v(N=0) == 0 and v(K=0) == 0
+    c = lambda acc=F: lib.kda_decode_commit(F, F, F, F, F, F, acc, 2, 3, 2, 128, 128, None)
+    assert c(acc=None) == 1
