@@ -1140,8 +1140,8 @@ int segment_chunks(int nc_max) {
 }
 
 // The overlapped schedule pays off for sequences of at least 128 chunks
-// (8192 tokens) and few states: stage 2 must leave stage 1 at least half
-// the SMs.
+// (8192 tokens) and few long-lived state chains: stage 2 must leave stage 1
+// at least half the SMs.
 bool use_overlap(int n_states, int nc_max, int sms) {
   return n_states <= sms / 2 && nc_max >= 128;
 }
@@ -1198,8 +1198,14 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // fill the other SMs while it runs; that stage's grid completes only after
   // the state pass (its last CTA waits for it), so every state pass starts
   // after both the records of its segment and the state carried into it.
+  // Stage-2 CTAs that stay resident for most of the call: every (sequence,
+  // head) for fixed lengths; for packed sequences about H per multiple of the
+  // longest length (short sequences' chains end early and give their SMs back).
+  const int long_chains = pr.cu_seqlens
+      ? pr.H * (int)(((long long)pr.T_total + pr.T - 1) / std::max(pr.T, 1))
+      : pr.n_seq * pr.H;
   const bool overlap = allow_overlap && carry && grid_done &&
-                       use_overlap(pr.n_seq * pr.H, nc_max, sms);
+                       use_overlap(long_chains, nc_max, sms);
   if (!overlap) {
     e = intra(0, nc_max, false);
     if (e == cudaSuccess) e = state(0, nc_max);
