@@ -118,82 +118,120 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
 // and the state after the last applied token is written when state_out is
 // given.  Verify: counts = null, state_out = null (the state is only read).
 // Commit: counts = accepted, state_out = state, out = null.
-template <typename OutT>
+// Several tokens per (sequence, head) in order.  The state stays in registers
+// across the tokens, so it is read once and written once (or not at all, for
+// verification) however many tokens there are.  Each CTA owns d_v / SPLIT
+// value columns: thread t holds columns [4 j, 4 j + 4) of them (j = t % TJ)
+// for rows [RPT g, RPT g + RPT) (g = t / TJ).  Measured at 256 sequences x
+// 32 heads x 4 tokens, halves beat quarters and eighths of d_v: each token's
+// barriers and column sums cost the same per CTA whatever its width, so
+// narrower CTAs only add CTAs.
+template <typename OutT, int SPLIT>
 __global__ void __launch_bounds__(128) decode_tokens_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ log_alpha,
     const __nv_bfloat16* __restrict__ beta, const float* state_in, float* state_out,
     OutT* __restrict__ out, const int* __restrict__ counts, int K, int H, float scale) {
-  __shared__ float s_alpha[DK], s_k[DK], s_q[DK];
-  __shared__ float s_part[2][8][HALF];
-  __shared__ float s_kq[4];
-  __shared__ float s_u[HALF];
+  constexpr int COLS = DV / SPLIT;  // value columns of this CTA
+  constexpr int TJ = COLS / 4;      // threads across a row (one float4 each)
+  constexpr int G = 128 / TJ;       // row groups
+  constexpr int RPT = DK / G;       // rows per thread
+  // The tokens' activations are staged KT at a time, all loads issued
+  // together, so a pass pays one global-memory latency rather than one per
+  // token.
+  constexpr int KT = 8;
+  __shared__ float s_alpha[KT][DK], s_k[KT][DK], s_q[KT][DK];
+  __shared__ float s_v[KT][COLS], s_beta[KT], s_kq[KT][4];
+  __shared__ float s_part[2][G][COLS];
+  __shared__ float s_u[COLS];
 
   const int tid = threadIdx.x;
-  const int nh = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int nh = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
   const int n = nh / H, h = nh - n * H;
   const int steps = counts ? min(max(counts[n], 0), K) : K;
-  const int j = tid & 15, g = tid >> 4;
+  const int j = tid % TJ, g = tid / TJ;
   constexpr int ROW_F4 = DV / 4;
   const size_t s_off = (size_t)nh * DK * DV;
-  const float4* Sin = reinterpret_cast<const float4*>(state_in + s_off) + half * (HALF / 4) + j;
+  const float4* Sin = reinterpret_cast<const float4*>(state_in + s_off) + part * TJ + j;
 
-  float4 s[ROWS_PER_THREAD];
+  float4 s[RPT];
 #pragma unroll
-  for (int i = 0; i < ROWS_PER_THREAD; ++i) s[i] = Sin[(size_t)(g * ROWS_PER_THREAD + i) * ROW_F4];
+  for (int i = 0; i < RPT; ++i) s[i] = Sin[(size_t)(g * RPT + i) * ROW_F4];
 
-  for (int t = 0; t < steps; ++t) {
-    const size_t row = (size_t)(n * K + t) * H + h;  // (n, t, h)
-    __syncthreads();  // the previous token's readers of the shared vectors are done
-    {
-      const float la = __bfloat162float(log_alpha[row * DK + tid]);
-      const float kc = __bfloat162float(k[row * DK + tid]);
-      const float qc = __bfloat162float(q[row * DK + tid]);
-      s_alpha[tid] = expf(la);
-      s_k[tid] = kc;
-      s_q[tid] = qc;
-      float kq = kc * qc;
+  for (int t0 = 0; t0 < steps; t0 += KT) {
+    const int nt = min(KT, steps - t0);
+    __syncthreads();  // the previous pass's readers of the staged tokens are done
+    __nv_bfloat16 r_la[KT], r_k[KT], r_q[KT], r_v[KT], r_b[KT];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
-      if ((tid & 31) == 0) s_kq[tid >> 5] = kq;
-    }
-    __syncthreads();
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-#pragma unroll
-    for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-      const int c = g * ROWS_PER_THREAD + i;
-      const float al = s_alpha[c], kc = s_k[c], qc = s_q[c];
-      s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
-      a.x += s[i].x * kc; a.y += s[i].y * kc; a.z += s[i].z * kc; a.w += s[i].w * kc;
-      b.x += s[i].x * qc; b.y += s[i].y * qc; b.z += s[i].z * qc; b.w += s[i].w * qc;
-    }
-    *reinterpret_cast<float4*>(&s_part[0][g][4 * j]) = a;
-    *reinterpret_cast<float4*>(&s_part[1][g][4 * j]) = b;
-    __syncthreads();
-    if (tid < HALF) {
-      float at = 0.f, bt = 0.f;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        at += s_part[0][r][tid];
-        bt += s_part[1][r][tid];
+    for (int t = 0; t < KT; ++t) {
+      if (t < nt) {
+        const size_t row = (size_t)(n * K + t0 + t) * H + h;  // (n, t0 + t, h)
+        r_la[t] = log_alpha[row * DK + tid];
+        r_k[t] = k[row * DK + tid];
+        r_q[t] = q[row * DK + tid];
+        if (tid < COLS) r_v[t] = v[row * DV + part * COLS + tid];
+        if (tid == 0) r_b[t] = beta[row];
       }
-      const int col = half * HALF + tid;
-      const float u = __bfloat162float(beta[row]) * (__bfloat162float(v[row * DV + col]) - at);
-      s_u[tid] = u;
-      if (out) store_out(out + row * DV + col, scale * (bt + u * (s_kq[0] + s_kq[1] + s_kq[2] + s_kq[3])));
+    }
+#pragma unroll
+    for (int t = 0; t < KT; ++t) {
+      if (t < nt) {
+        const float kc = __bfloat162float(r_k[t]), qc = __bfloat162float(r_q[t]);
+        s_alpha[t][tid] = expf(__bfloat162float(r_la[t]));
+        s_k[t][tid] = kc;
+        s_q[t][tid] = qc;
+        if (tid < COLS) s_v[t][tid] = __bfloat162float(r_v[t]);
+        if (tid == 0) s_beta[t] = __bfloat162float(r_b[t]);
+        float kq = kc * qc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        if ((tid & 31) == 0) s_kq[t][tid >> 5] = kq;
+      }
     }
     __syncthreads();
-    const float4 u = *reinterpret_cast<const float4*>(&s_u[4 * j]);
+    for (int t = 0; t < nt; ++t) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
 #pragma unroll
-    for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-      const float kc = s_k[g * ROWS_PER_THREAD + i];
-      s[i].x += kc * u.x; s[i].y += kc * u.y; s[i].z += kc * u.z; s[i].w += kc * u.w;
+      for (int i = 0; i < RPT; ++i) {
+        const int c = g * RPT + i;
+        const float al = s_alpha[t][c], kc = s_k[t][c], qc = s_q[t][c];
+        s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
+        a.x += s[i].x * kc; a.y += s[i].y * kc; a.z += s[i].z * kc; a.w += s[i].w * kc;
+        b.x += s[i].x * qc; b.y += s[i].y * qc; b.z += s[i].z * qc; b.w += s[i].w * qc;
+      }
+      *reinterpret_cast<float4*>(&s_part[0][g][4 * j]) = a;
+      *reinterpret_cast<float4*>(&s_part[1][g][4 * j]) = b;
+      __syncthreads();
+      if (tid < COLS) {
+        float at = 0.f, bt = 0.f;
+#pragma unroll
+        for (int r = 0; r < G; ++r) {
+          at += s_part[0][r][tid];
+          bt += s_part[1][r][tid];
+        }
+        const float u = s_beta[t] * (s_v[t][tid] - at);
+        s_u[tid] = u;
+        if (out) {
+          const size_t row = (size_t)(n * K + t0 + t) * H + h;
+          const float kq = s_kq[t][0] + s_kq[t][1] + s_kq[t][2] + s_kq[t][3];
+          store_out(out + row * DV + part * COLS + tid, scale * (bt + u * kq));
+        }
+      }
+      __syncthreads();
+      const float4 u = *reinterpret_cast<const float4*>(&s_u[4 * j]);
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float kc = s_k[t][g * RPT + i];
+        s[i].x += kc * u.x; s[i].y += kc * u.y; s[i].z += kc * u.z; s[i].w += kc * u.w;
+      }
+      // No barrier here: the next token writes s_part only after every thread
+      // has read s_u, and s_u only after the next token's first barrier.
     }
   }
   if (state_out) {
-    float4* Sout = reinterpret_cast<float4*>(state_out + s_off) + half * (HALF / 4) + j;
+    float4* Sout = reinterpret_cast<float4*>(state_out + s_off) + part * TJ + j;
 #pragma unroll
-    for (int i = 0; i < ROWS_PER_THREAD; ++i) Sout[(size_t)(g * ROWS_PER_THREAD + i) * ROW_F4] = s[i];
+    for (int i = 0; i < RPT; ++i) Sout[(size_t)(g * RPT + i) * ROW_F4] = s[i];
   }
 }
 
@@ -203,16 +241,17 @@ cudaError_t launch_decode_tokens(const void* q, const void* k, const void* v,
                                  const void* log_alpha, const void* beta, const float* state_in,
                                  float* state_out, void* out, bool out_f32, const int* counts,
                                  int N, int K, int H, float scale, cudaStream_t stream) {
-  const long long blocks = 2LL * N * H;
+  constexpr int SPLIT = 2;
+  const long long blocks = (long long)SPLIT * N * H;
   if (blocks == 0 || K == 0) return cudaSuccess;
   const dim3 grid((unsigned)blocks);
   auto bf = [](const void* p) { return static_cast<const __nv_bfloat16*>(p); };
   if (out_f32 || !out)
-    decode_tokens_kernel<float><<<grid, 128, 0, stream>>>(
+    decode_tokens_kernel<float, SPLIT><<<grid, 128, 0, stream>>>(
         bf(q), bf(k), bf(v), bf(log_alpha), bf(beta), state_in, state_out,
         static_cast<float*>(out), counts, K, H, scale);
   else
-    decode_tokens_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
+    decode_tokens_kernel<__nv_bfloat16, SPLIT><<<grid, 128, 0, stream>>>(
         bf(q), bf(k), bf(v), bf(log_alpha), bf(beta), state_in, state_out,
         static_cast<__nv_bfloat16*>(out), counts, K, H, scale);
   return cudaGetLastError();

@@ -25,8 +25,9 @@ def _draft(N, K, H, seed):
     return gen.make_inputs(N, K, H, 128, 128, seed=seed, init_std=0.02)
 
 
+# K = 19 stages the drafted tokens in three passes, the last one ragged
 @pytest.mark.parametrize("N,K,H,out_dtype", [(5, 4, 3, torch.float32), (8, 7, 2, torch.bfloat16),
-                                              (3, 1, 2, torch.float32)])
+                                              (3, 1, 2, torch.float32), (3, 19, 2, torch.float32)])
 def test_verify_matches_oracle_and_leaves_state(N, K, H, out_dtype):
     x = _draft(N, K, H, seed=70 + K)
     g = {k: v.cuda() for k, v in x.items()}
@@ -43,11 +44,14 @@ def test_verify_matches_oracle_and_leaves_state(N, K, H, out_dtype):
         assert_output_close(out, ro)
 
 
-def test_commit_matches_oracle_per_accepted_count():
-    N, K, H = 6, 5, 2
-    x = _draft(N, K, H, seed=80)
+# counts above K are clamped to K; with K = 13 the accepted counts end inside
+# the first and second staging passes and on their boundary
+@pytest.mark.parametrize("K,acc", [(5, [0, 1, 2, 5, 3, 9]), (13, [0, 8, 9, 13, 20, 4])])
+def test_commit_matches_oracle_per_accepted_count(K, acc):
+    N, H = 6, 2
+    x = _draft(N, K, H, seed=80 + K)
     g = {k: v.cuda() for k, v in x.items()}
-    acc = np.array([0, 1, 2, 5, 3, 9], dtype=np.int32)  # 9 is clamped to K
+    acc = np.array(acc, dtype=np.int32)
     s = g["initial_state"].clone()
     binding.kda_decode_commit(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], s,
                               torch.from_numpy(acc).cuda())
