@@ -15,11 +15,12 @@
 // architecture", section "Eine Untergrenze, die einen GPU-Codepfad
 // beseitigte"), has to divide by the accumulated decay.  With log_alpha in
 // [-5, 0], the log-decay across a 16-token tile spans at most 80, so for a
-// column tile b with end reference E_b = g at its last token,
-//   e^{g_r - g_i} = e^{g_r - E_b} * e^{E_b - g_i},   i in tile b, r >= i,
-// has a left factor in [0, e^80] and a right factor in [e^-80, 1]: both fit
-// bf16/fp32.  So the DIAGONAL tiles use the same dense tcgen05 product as
-// the off-diagonal ones; there is no per-position-pair special path.
+// row tile a with reference R_a = g just before its first token,
+//   e^{g_r - g_i} = e^{g_r - R_a} * e^{R_a - g_i},   r in tile a, i <= r,
+// has a left factor in [e^-80, 1] and a right factor in [1, e^80] on the
+// diagonal tile (at most 1 before it): both fit the fp32 exponent.  So the
+// DIAGONAL tiles use the same dense tcgen05 product as the off-diagonal
+// ones; there is no per-position-pair special path.
 //
 // Stage 1 (kda_intra_kernel) needs no state, so it runs one CTA per
 // (chunk, head) over every SM (two CTAs per SM).  It writes a per-chunk
@@ -38,7 +39,9 @@
 //   the cumulative sum g^T = LA^T L^T (L lower-triangular ones) and the
 //   transposes q^T = Q^T I, k^T = K^T I move per-channel columns into TMEM
 //   (one thread per key channel reads them back);
-//   M1 (x4) [Q^(b); K^(b)] . Kb[tile b]^T -> column tile b of [A_qk; A_kk];
+//   M1 (x2) K~ . [Q~; K~]^T -> A_qk^T, A_kk^T, keys on TMEM lanes: one
+//   product stacks the key operands of row tiles 3 and 2 (64 + 48 keys)
+//   on M, the other those of row tiles 1 and 0 (32 + 16 keys);
 //   M2 (k e^g)^T (T diag beta)^T -> W^T.
 // The 64x64 unit lower-triangular inverse is formed in fp32 on CUDA cores.
 //
@@ -53,6 +56,7 @@
 //
 // d = 64 heads run the d = 128 code with the upper channel half zeroed.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -76,7 +80,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t REC_WT = 0;         // W (fp16), B operand: N = r, K = c, MN-major
 constexpr uint32_t REC_QT = 16384;     // q e^g (fp16), B operand: N = r, K = c, MN-major
 constexpr uint32_t REC_KBAR = 32768;   // k e^{g_C - g} (fp16), B operand: N = c, K = i
-constexpr uint32_t REC_AQ = 49152;     // A_qk (fp16), B operand: N = r, K = i
+constexpr uint32_t REC_AQ = 49152;     // A_qk (fp16), B operand: N = r, K = i, MN-major
 constexpr uint32_t REC_TB = 57344;     // T diag(beta) (bf16), B operand: N = r, K = i
 constexpr uint32_t REC_G = 65536;      // e^{g_C} per key channel, fp32 x 128
 constexpr uint32_t REC_LOAD = 66048;   // bytes copied per record
@@ -185,12 +189,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 
 __device__ __forceinline__ void set_status(int code) { atomicExch(&g_chunk_status, code); }
 
-// Version b of the M1 A operand: rows r >= 16 b of [Q^(b); K^(b)] with
-// Q^(b)_rc = q_rc e^{g_rc - E_bc} = q_rc p_r e^{E_a - E_b} (a = tile of r; same
-// for K), rounded to tf32 (K-major fp32: a thread writes column c of every
-// row it owns, a warp one 128-byte line).  The calling thread builds the rows
-// of its two tiles ta[0], ta[1] (with p and Eo their p and tile ends).  Rows
-// above 16 b are never read back.
 // Address of element (row, channel c) of a K-major, 128-byte-swizzled fp32
 // operand: cbase = base + (c / 32) * kb_stride, cl = (c % 32) * 4.  Row
 // groups of 8 are 1024 bytes apart; the swizzle XORs the 16-byte chunk
@@ -201,26 +199,57 @@ __device__ __forceinline__ uint32_t kmaj32_addr(uint32_t cbase, uint32_t cl, int
          (cl ^ ((uint32_t)(row & 7) << 4));
 }
 
-template <int B>
-__device__ __forceinline__ void build_version(uint32_t xbase, uint32_t cl, uint32_t tl,
-                                              const float (&p)[2][16], const float (&Eo)[2],
-                                              float EB, const int (&ta)[2]) {
+// M1 operands of one round, kind::tf32 (fp32 rounded to nearest tf32).
+// Row tile a is referenced to R_a, the log-decay just before it (E_{a-1},
+// and 0 for a = 0):
+//   e^{g_r - g_i} = e^{g_r - R_a} e^{R_a - g_i},   r in tile a, i <= r.
+// The left factor lies in [e^-80, 1].  The right one lies in [1, e^80] for
+// keys of tile a and is at most 1 for earlier keys, where it may underflow
+// to zero: the exact product is then smaller still.
+//   A operand, M = 128 key rows, K~^(a)_i = k_i e^{R_a - g_i}: round 0 holds
+//     row tile 3's keys 0..63 in rows 0..63 and row tile 2's keys 0..47 in
+//     rows 64..111; round 1 row tile 1's keys 0..31 in rows 0..31 and row
+//     tile 0's keys 0..15 in rows 32..47.
+//   B operand, N = 64 token rows, q_r e^{g_r - R_a} and k_r e^{g_r - R_a}
+//     of the round's row tiles: rows 0..15 / 16..31 q / k of the odd tile
+//     (3 or 1), rows 32..47 / 48..63 q / k of the even tile (2 or 0).
+// A rows left unwritten reach only TMEM lanes that are never read.  The
+// calling thread writes channel c of the rows of its tiles ta[0], ta[1]
+// (p: their e^{g - E}), one element per row, a warp one 128-byte line.
+// E: every tile's end; Eo, Ep: the end of tile ta[s] and of the tile before
+// it (0 for tile 0).
+template <int R>
+__device__ __forceinline__ void build_round(uint32_t abase, uint32_t bbase, uint32_t cl,
+                                            uint32_t tl, const float (&p)[2][16],
+                                            const float (&E)[4], const float (&Eo)[2],
+                                            const float (&Ep)[2], const int (&ta)[2]) {
+  constexpr int AHI = R == 0 ? 3 : 1, ALO = AHI - 1;  // the round's row tiles
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const int a = ta[s];
-    if (a < B) continue;  // warp-uniform
-    float qv[16], kv[16];
-    tmem_ld16(tl + TA_Q + 16 * a, qv);
-    tmem_ld16(tl + TA_K + 16 * a, kv);
+    const int t = ta[s];
+    if (t > AHI) continue;           // warp-uniform
+    const bool rows = t >= ALO;      // t is one of the round's row tiles
+    float kv[16], qv[16];
+    tmem_ld16(tl + TA_K + 16 * t, kv);
+    if (rows) tmem_ld16(tl + TA_Q + 16 * t, qv);
     tmem_ld_wait();
-    const float fab = ex2((Eo[s] - EB) * LOG2E);  // e^{E_a - E_b} in [e^-240, 1]
-    const uint32_t qrow = xbase + ((uint32_t)a << 11);  // rows 16 a .. 16 a + 15
+    const float et = Eo[s];
+    const float f_hi = ex2((E[AHI - 1] - et) * LOG2E);                   // e^{R_AHI - E_t}
+    const float f_lo = ex2(((ALO > 0 ? E[ALO - 1] : 0.f) - et) * LOG2E);  // e^{R_ALO - E_t}
+    const float f_b = ex2((et - Ep[s]) * LOG2E);                          // e^{E_t - R_t}
+    const uint32_t a_hi = abase + ((uint32_t)t << 11);
+    const uint32_t a_lo = abase + ((uint32_t)((R == 0 ? 4 : 2) + t) << 11);
+    const uint32_t b_q = bbase + ((uint32_t)((t & 1) ? 0 : 2) << 11);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float f = p[s][j] * fab;
-      const uint32_t at = kmaj32_addr(qrow, cl, j);
-      st_f32(at, tf32r(qv[j] * f));
-      st_f32(at + (CH / 8) * 1024, tf32r(kv[j] * f));  // row CH + 16 a + j
+      const float kr = kv[j] * rcp(p[s][j]);  // k e^{E_t - g}
+      st_f32(kmaj32_addr(a_hi, cl, j), tf32r(kr * f_hi));
+      if (t <= ALO) st_f32(kmaj32_addr(a_lo, cl, j), tf32r(kr * f_lo));
+      if (rows) {
+        const float f = p[s][j] * f_b;  // e^{g - R_t}
+        st_f32(kmaj32_addr(b_q, cl, j), tf32r(qv[j] * f));
+        st_f32(kmaj32_addr(b_q + 2048, cl, j), tf32r(kv[j] * f));
+      }
     }
   }
 }
@@ -230,51 +259,99 @@ __device__ __forceinline__ int tix(int r, int c) {
   return r * CH + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
 }
 
-// Off-diagonal blocks at distance S: T_ab = -T_aa sum_{m=b}^{a-1} L_am T_mb
-// for a - b = S.  akk holds L transposed (akk[i][r] = L[r][i]); dinv[a][x][rr]
-// = T_aa[rr][x]; P goes to the unused upper-triangle block (b, a) of ti.
-template <int S>
-__device__ __forceinline__ void solve_level(const float* akk, float* ti, const float* dinv,
-                                            int tid) {
-  constexpr int kStrips = (4 - S) * 64;  // (block, row, 4-column quad)
+// The off-diagonal blocks of T from its diagonal blocks, by halves.  akk
+// holds L transposed (akk[i][r] = L[r][i]); dinv[a][x][rr] = T_aa[rr][x].
+// With T1, T2 the inverses of the two 32 x 32 diagonal halves of L and L_C
+// its lower-left 32 x 32 block,
+//   T1 = [T_00 0; T_10 T_11],  T_10 = -T_11 L_10 T_00  (T_32 likewise),
+//   lower-left block of T = -T2 (L_C T1).
+// Four phases: P = L_{b+1,b} T_bb and T_{b+1,b} = -T_{b+1,b+1} P for b = 0
+// and 2 (P in the unused block (b, b+1) of ti), then X = L_C T1 (block
+// (kb, cb) of X in the unused block (cb, kb)), then -T2 X.  A thread owns a
+// strip of 4 columns of one row; each phase ends in a CTA barrier.
+__device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const float* dinv,
+                                              int tid) {
+  if (tid < 128) {
+    const int b = 2 * (tid >> 6), a = b + 1, rr = (tid >> 2) & 15, q = tid & 3;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int st = tid; st < kStrips; st += A_THREADS) {
-    const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-    for (int mm = 0; mm < S; ++mm) {
-      const int m = b + mm;
-#pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const float l = akk[(16 * m + x) * CH + 16 * a + rr];
-        const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * m + x, 16 * b + 4 * q));
-        acc0 += l * t.x;
-        acc1 += l * t.y;
-        acc2 += l * t.z;
-        acc3 += l * t.w;
-      }
+    for (int x = 0; x < 16; ++x) {
+      const float l = akk[(16 * b + x) * CH + 16 * a + rr];
+      const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * b + x, 16 * b + 4 * q));
+      acc.x += l * t.x;
+      acc.y += l * t.y;
+      acc.z += l * t.z;
+      acc.w += l * t.w;
     }
-    *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) =
-        make_float4(acc0, acc1, acc2, acc3);
+    *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) = acc;
   }
   __syncthreads();
-#pragma unroll
-  for (int st = tid; st < kStrips; st += A_THREADS) {
-    const int b = st >> 6, a = b + S, rr = (st >> 2) & 15, q = st & 3;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+  if (tid < 128) {
+    const int b = 2 * (tid >> 6), a = b + 1, rr = (tid >> 2) & 15, q = tid & 3;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int x = 0; x < 16; ++x) {
       const float d = dinv[(a * 16 + x) * 16 + rr];
       const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * b + x, 16 * a + 4 * q));
-      acc0 += d * t.x;
-      acc1 += d * t.y;
-      acc2 += d * t.z;
-      acc3 += d * t.w;
+      acc.x += d * t.x;
+      acc.y += d * t.y;
+      acc.z += d * t.z;
+      acc.w += d * t.w;
     }
     *reinterpret_cast<float4*>(ti + tix(16 * a + rr, 16 * b + 4 * q)) =
-        make_float4(-acc0, -acc1, -acc2, -acc3);
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
+  {  // X = L_C T1: rows r in [32, 64), columns of block cb; T1 is zero above its diagonal blocks
+    const int cb = tid >> 7, r = 32 + ((tid >> 2) & 31), c0 = 16 * cb + 4 * (tid & 3);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto term = [&](int m) {
+      const float l = akk[m * CH + r];
+      const float4 t = *reinterpret_cast<const float4*>(ti + tix(m, c0));
+      acc.x += l * t.x;
+      acc.y += l * t.y;
+      acc.z += l * t.z;
+      acc.w += l * t.w;
+    };
+    if (cb == 0) {  // warp-uniform
+#pragma unroll
+      for (int m = 0; m < 16; ++m) term(m);
+    }
+#pragma unroll
+    for (int m = 16; m < 32; ++m) term(m);
+    *reinterpret_cast<float4*>(ti + tix(16 * cb + (r & 15), 16 * (r >> 4) + (c0 & 15))) = acc;
+  }
+  __syncthreads();
+  {  // -T2 X: rows r of block 2 + rb, columns of block cb; T2 is zero above its diagonal blocks
+    const int rb = tid >> 7, cb = (tid >> 6) & 1;
+    const int r = 32 + 16 * rb + ((tid >> 2) & 15), c0 = 16 * cb + 4 * (tid & 3);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto term = [&](int k) {
+      const float t2 = ti[tix(r, k)];
+      const float4 x = *reinterpret_cast<const float4*>(ti + tix(16 * cb + (k & 15), 16 * (k >> 4) + 4 * (tid & 3)));
+      acc.x += t2 * x.x;
+      acc.y += t2 * x.y;
+      acc.z += t2 * x.z;
+      acc.w += t2 * x.w;
+    };
+#pragma unroll
+    for (int k = 32; k < 48; ++k) term(k);
+    if (rb == 1) {  // warp-uniform
+#pragma unroll
+      for (int k = 48; k < 64; ++k) term(k);
+    }
+    *reinterpret_cast<float4*>(ti + tix(r, c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+}
+
+// Position pair pidx of the ablation: tile a, row rr and column ii <= rr.
+__device__ __forceinline__ void pair_of(int pidx, int& a, int& rr, int& ii) {
+  a = pidx / 136;
+  const int idx = pidx - 136 * a;
+  rr = 0;
+  while ((rr + 1) * (rr + 2) / 2 <= idx) ++rr;
+  ii = idx - rr * (rr + 1) / 2;
 }
 
 // Ablation of the dense diagonal tiles: the four 16x16 diagonal tiles of
@@ -284,13 +361,13 @@ __device__ __forceinline__ void solve_level(const float* akk, float* ti, const f
 // (the orkas.ai page, "Kimi K3 architecture", section "Eine Untergrenze,
 // die einen GPU-Codepfad beseitigte", describes the previous generation's
 // kernels keeping such a path for the diagonal).  q and k (exact in bf16)
-// and g (fp32) are staged as [token][channel] in [0, 64K) of shared memory,
-// which is free once M1 is done; one thread per position pair walks the
-// channels starting at a thread-dependent offset so a warp's loads fall in
-// distinct banks.  res[0..1023] receives A_qk and res[1024..2047] A_kk, as
-// [tile][r % 16][i % 16].  Called by all threads of the CTA.
-__device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
-                                                     float* res) {
+// and g (fp32) are staged as [token][channel] in [0, 64K) of shared memory;
+// one thread per position pair walks the channels starting at a
+// thread-dependent offset so a warp's loads fall in distinct banks.  Pair
+// pidx = tid + 256 n (of 4 x 136) leaves A_qk in aq[n] and A_kk in ak[n].
+// Called by all threads of the CTA.
+__device__ __forceinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
+                                                        float (&aq)[3], float (&ak)[3]) {
   uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
   uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
   float* sg = reinterpret_cast<float*>(sbp + 32768);
@@ -310,24 +387,25 @@ __device__ __noinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, 
     }
   }
   __syncthreads();
-#pragma unroll 1
-  for (int pidx = tid; pidx < 4 * 136; pidx += A_THREADS) {
-    const int a = pidx / 136, idx = pidx - 136 * a;
-    int rr = 0;
-    while ((rr + 1) * (rr + 2) / 2 <= idx) ++rr;
-    const int ii = idx - rr * (rr + 1) / 2;
-    const int r = 16 * a + rr, i = 16 * a + ii;
-    float aq = 0.f, ak = 0.f;
+#pragma unroll
+  for (int n = 0; n < 3; ++n) {
+    const int pidx = tid + A_THREADS * n;
+    float aqs = 0.f, aks = 0.f;
+    if (pidx < 4 * 136) {
+      int a, rr, ii;
+      pair_of(pidx, a, rr, ii);
+      const int r = 16 * a + rr, i = 16 * a + ii;
 #pragma unroll 4
-    for (int cc = 0; cc < DP; ++cc) {
-      const int ch = (cc + tid) & (DP - 1);
-      const float e = ex2((sg[r * DP + ch] - sg[i * DP + ch]) * LOG2E);
-      const float ki = bf2f(sk[i * DP + ch]) * e;
-      aq = fmaf(bf2f(sq[r * DP + ch]), ki, aq);
-      ak = fmaf(bf2f(sk[r * DP + ch]), ki, ak);
+      for (int cc = 0; cc < DP; ++cc) {
+        const int ch = (cc + tid) & (DP - 1);
+        const float e = ex2((sg[r * DP + ch] - sg[i * DP + ch]) * LOG2E);
+        const float ki = bf2f(sk[i * DP + ch]) * e;
+        aqs = fmaf(bf2f(sq[r * DP + ch]), ki, aqs);
+        aks = fmaf(bf2f(sk[r * DP + ch]), ki, aks);
+      }
     }
-    res[(16 * a + rr) * 16 + ii] = aq;
-    res[1024 + (16 * a + rr) * 16 + ii] = ak;
+    aq[n] = aqs;
+    ak[n] = aks;
   }
   __syncthreads();
 }
@@ -505,7 +583,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
 
   // ---- decay factors of this thread's channel and tiles: E[b] = g at the
   // end of tile b; p[s][j] = e^{g - E} of token 16 ta[s] + j, in [1, e^80]
-  float E[4], Eo[2], pr[2][16];
+  float E[4], Eo[2], Ep[2], pr[2][16];
   if (ok) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) E[b] = tmem_ld1(tl + TA_G + 16 * b + 15);
@@ -515,6 +593,8 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     tmem_ld_wait();
     Eo[0] = hh ? E[1] : E[0];
     Eo[1] = hh ? E[2] : E[3];
+    Ep[0] = hh ? E[0] : 0.f;
+    Ep[1] = hh ? E[1] : E[2];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       pr[0][j] = ex2((g0[j] - Eo[0]) * LOG2E);
@@ -522,103 +602,105 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     }
   }
 
-  // ---- M1: column tile b of [A_qk; A_kk], one tile version at a time.
-  // kind::tf32 with fp32 operands: A = version b, [128 rows][128 channels];
-  // B = K-bar, [64 keys][128 channels]; both K-major.
+  // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
+  // M1 operands (and the ablation's staging) below overwrite
+  if (tid == 0) bulk_wait_reads();
+  __syncthreads();
+  // ablation only: the diagonal tiles per position pair, while g is in TMEM
+  float pq[3], pk[3];
+  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, pq, pk);
+
+  // ---- M1 in two rounds of one kind::tf32 product each, K-major fp32
+  // operands: A = key rows under the references of two row tiles
+  // ([128 keys][128 channels]), B = those tiles' token rows ([64][128]).
+  // Round 0 writes TMEM columns TA_A, round 1 TA_G (g is no longer needed).
   OperandLayout XA = kmajor(sb + A_XH, 16384), KBA = kmajor(sb + A_KBH, 8192);
   XA.esize = 4;
   KBA.esize = 4;
-  constexpr uint32_t ID_M1 = make_idesc_tf32(128, 16, false, false);
-  // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
-  // M1 operands below overwrite
-  if (tid == 0) bulk_wait_reads();
-  __syncthreads();
+  constexpr uint32_t ID_M1 = make_idesc_tf32(128, 64, false, false);
   const uint32_t cl = (uint32_t)(c & 31) * 4;
-  const uint32_t xbase = sb + A_XH + (uint32_t)(c >> 5) * 16384;
-  if (ok) {  // K-bar = k e^{E - g} for this thread's tiles
-    const uint32_t kbase = sb + A_KBH + (uint32_t)(c >> 5) * 8192;
+  const uint32_t abase = sb + A_XH + (uint32_t)(c >> 5) * 16384;
+  const uint32_t bbase = sb + A_KBH + (uint32_t)(c >> 5) * 8192;
 #pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      float kv[16];
-      tmem_ld16(tl + TA_K + 16 * ta[s2], kv);
-      tmem_ld_wait();
-      const uint32_t krow = kbase + ((uint32_t)ta[s2] << 11);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        st_f32(kmaj32_addr(krow, cl, j), tf32r(kv[j] * rcp(pr[s2][j])));
-    }
-  }
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
+  for (int round = 0; round < 2; ++round) {
     if (!ok) break;
-    if (b == 0) build_version<0>(xbase, cl, tl, pr, Eo, E[0], ta);
-    if (b == 1) build_version<1>(xbase, cl, tl, pr, Eo, E[1], ta);
-    if (b == 2) build_version<2>(xbase, cl, tl, pr, Eo, E[2], ta);
-    if (b == 3) build_version<3>(xbase, cl, tl, pr, Eo, E[3], ta);
+    if (round == 0) build_round<0>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
+    if (round == 1) build_round<1>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
     operands_ready();
     if (tid == 0) {
-      const uint32_t d = tmem + TA_A + 16 * b;
+      const uint32_t d = tmem + (round == 0 ? TA_A : TA_G);
 #pragma unroll
       for (int k0 = 0; k0 < DP; k0 += 8)
-        umma_tf32(d, layout_desc(XA, 0, k0), layout_desc(KBA, 16 * b, k0), ID_M1, k0 > 0);
+        umma_tf32(d, layout_desc(XA, 0, k0), layout_desc(KBA, 0, k0), ID_M1, k0 > 0);
       umma_commit(bar_mma);
     }
     ok = wait_all(bar_mma, mma_phase);
   }
 
-  // per-pair diagonal tiles (ablation only), kept in the (k e^g)^T slot
-  float* s_pair = reinterpret_cast<float*>(sbp + A_KT);
-  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, s_pair);
-
   float* akk = reinterpret_cast<float*>(sbp + A_AKK);
   float* ti = reinterpret_cast<float*>(sbp + A_TI);
-  const OperandLayout AQ = kmajor(sb + A_STG + REC_AQ, 0);
+  const OperandLayout AQ = mnmajor(sb + A_STG + REC_AQ, 8192);
   const OperandLayout QT = mnmajor(sb + A_STG + REC_QT, 16384);
   const OperandLayout KBAR = kmajor(sb + A_STG + REC_KBAR, 0);
   const OperandLayout KT = kmajor(sb + A_KT, 0);
   const OperandLayout TB = kmajor(sb + A_STG + REC_TB, 0);
   const OperandLayout WT = mnmajor(sb + A_WST, 16384);
   if (ok) {
-    // ---- A_qk (fp16 record image) and beta-scaled strictly-lower A_kk (fp32):
-    // TMEM lane c is row c of [A_qk; A_kk]; this thread takes columns
-    // [32 hh, 32 hh + 32).
-    {
-      const int i_lo = 32 * hh;
-      float a0[16], a1[16];
-      tmem_ld16(tl + TA_A + i_lo, a0);
-      tmem_ld16(tl + TA_A + i_lo + 16, a1);
+    // ---- A_qk (fp16 record image, MN-major: N = r, K = i) and beta-scaled
+    // strictly-lower A_kk (fp32, stored transposed, akk[i][r] = L[r][i]: the
+    // solve reads L by columns, and an unswizzled row keeps its addresses
+    // compile-time offsets; the stores here conflict, the solve's loads do not).  TMEM lane = key: round 0 (TA_A) lanes 0..63 are the keys
+    // of row tile 3 and lanes 64..111 keys 0..47 of row tile 2; round 1
+    // (TA_G) lanes 0..31 keys of row tile 1 and lanes 32..47 keys 0..15 of
+    // row tile 0.  Columns: q then k rows of the odd tile, then of the even
+    // one.  hh = 0 takes the q columns (A_qk), hh = 1 the k columns (A_kk).
+    auto extract = [&](uint32_t cols, int a, int i) {
+      float v[16];
+      tmem_ld16(tl + cols + ((a & 1) ? 0 : 32) + 16 * hh, v);
       tmem_ld_wait();
-      float a[32];
+      if (i >= 16 * (a + 1)) return;  // a key after the row tile
+      if (hh == 0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        a[j] = a0[j];
-        a[16 + j] = a1[j];
-      }
-      const int r = c < CH ? c : c - CH;
-      if (PAIRS && ((r >> 5) == hh)) {  // this row's diagonal tile from the per-pair path
-        const float* row = s_pair + (c < CH ? 0 : 1024) + (r >> 4) * 256 + (r & 15) * 16;
-        const int o = 16 * ((r >> 4) & 1);  // offset of the diagonal tile in a[]
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          if (jj <= (r & 15)) {
-            if (o == 0) a[jj] = row[jj]; else a[16 + jj] = row[jj];
-          }
-      }
-      if (c < CH) {
-#pragma unroll
-        for (int i0 = 0; i0 < 32; i0 += 8) {
+        for (int h8 = 0; h8 < 16; h8 += 8) {
           float x[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = (i_lo + i0 + j <= r) ? a[i0 + j] : 0.f;
-          st8h(layout_addr(AQ, r, i_lo + i0), x);
+          for (int j = 0; j < 8; ++j) x[j] = i <= 16 * a + h8 + j ? v[h8 + j] : 0.f;
+          st8h(layout_addr(AQ, 16 * a + h8, i), x);
         }
-      } else {  // stored transposed, akk[i][r] = L[r][i]: the solve reads L by columns
-        const float br = s_beta[r];
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) akk[(i_lo + i) * CH + r] = (i_lo + i < r) ? br * a[i] : 0.f;
+        for (int q4 = 0; q4 < 16; q4 += 4) {
+          const int r0 = 16 * a + q4;
+          float4 x;
+          x.x = i < r0 ? s_beta[r0] * v[q4] : 0.f;
+          x.y = i < r0 + 1 ? s_beta[r0 + 1] * v[q4 + 1] : 0.f;
+          x.z = i < r0 + 2 ? s_beta[r0 + 2] * v[q4 + 2] : 0.f;
+          x.w = i < r0 + 3 ? s_beta[r0 + 3] * v[q4 + 3] : 0.f;
+          *reinterpret_cast<float4*>(akk + i * CH + r0) = x;
+        }
+      }
+    };
+    const int quad = c >> 5;  // warp-uniform
+    extract(TA_A, quad < 2 ? 3 : 2, c & 63);
+    if (quad < 2) extract(TA_G, quad == 0 ? 1 : 0, c & 31);
+    if (hh == 0 && c < CH) {  // A_qk is zero above the diagonal tiles
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int r0 = 0; r0 < 16 * (c >> 4); r0 += 8) st8h(layout_addr(AQ, r0, c), z);
+    }
+    if (PAIRS) {  // the ablation's diagonal tiles replace the dense ones
+      __syncthreads();
+#pragma unroll
+      for (int n = 0; n < 3; ++n) {
+        const int pidx = tid + A_THREADS * n;
+        if (pidx < 4 * 136) {
+          int a, rr, ii;
+          pair_of(pidx, a, rr, ii);
+          const int r = 16 * a + rr, i = 16 * a + ii;
+          *reinterpret_cast<__half*>(sbp + (layout_addr(AQ, r, i) - sb)) = __float2half_rn(pq[n]);
+          if (ii < rr) akk[i * CH + r] = s_beta[r] * pk[n];
+        }
       }
     }
-    if (PAIRS) __syncthreads();  // s_pair is overwritten by (k e^g)^T below
     // ---- (k e^g)^T (bf16, M2 operand), q e^g and k e^{g_C - g} (fp16 record
     // images), for this thread's channel and tiles
 #pragma unroll
@@ -678,11 +760,8 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       for (int q = 0; q < 4; ++q) drow[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
     __syncthreads();
-    // off-diagonal blocks by distance s = a - b: P = sum_{m=b}^{a-1} L_am T_mb,
-    // then T_ab = -T_aa P.  A thread owns a strip of 4 columns of one row.
-    solve_level<1>(akk, ti, dinv, tid);
-    solve_level<2>(akk, ti, dinv, tid);
-    solve_level<3>(akk, ti, dinv, tid);
+    // off-diagonal blocks: T_10 and T_32, then the lower-left 32 x 32 block
+    solve_offdiag(akk, ti, dinv, tid);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
       const int r = tid >> 2, i_lo = (tid & 3) * 16;
@@ -882,7 +961,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     if ((tid & 31) == 0 && nchunks > 0) {
       constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
       constexpr uint32_t ID_D = make_idesc(128, 128, false, true, true, true);    // fp16, -A
-      constexpr uint32_t ID_O2 = make_idesc(128, 64, false, false, true, true);   // fp16, -A
+      constexpr uint32_t ID_O2 = make_idesc(128, 64, false, true, true, true);    // fp16, -A
       constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
       // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is
       // issued as soon as record j lands, ahead of the chain's own products.
@@ -926,7 +1005,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         tc_fence_after_sync();
         {
           const uint64_t dut = layout_desc(UT, 0, 0);
-          const uint64_t daq = layout_desc(kmajor(rb + REC_AQ, 0), 0, 0);
+          const uint64_t daq = layout_desc(mnmajor(rb + REC_AQ, 8192), 0, 0);
           const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
           // M6 first: the chain waits only for the state update; the second
           // half of M5 (the output) runs while the chain rebuilds S^T
@@ -936,7 +1015,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
           umma_commit(mma_b);
 #pragma unroll
           for (int k0 = 0; k0 < CH; k0 += 16)
-            umma_bf16(td + 64, desc_adv(dut, k0, false), desc_adv(daq, k0, false), ID_O2, 1);
+            umma_bf16(td + 64, desc_adv(dut, k0, false), desc_adv(daq, k0, true), ID_O2, 1);
           umma_commit(&o_full[ob]);
         }
         if (j + 2 < nchunks) {  // buffer buf is consumed once every product of chunk j is done
