@@ -420,7 +420,10 @@ struct IntraParams {
   int T, n_seq, H;
   int check_decay;
   int j_lo, seg_len, n_items;
-  int* grid_done;  // launched as a dependent of a state pass: CTAs finished, else null
+  // Overlapped schedule, else null: grid_done[0] counts finished CTAs,
+  // grid_done[1] hands out items to a persistent grid.  The CTA that
+  // finishes last resets both.
+  int* grid_done;
 };
 
 template <int DIN, bool PAIRS>
@@ -503,7 +506,19 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     it.valid = min(CH, len - CH * jc);
     return it;
   };
-  for (int w = blockIdx.x; ok && w < p.n_items; w += gridDim.x) {
+  int* s_item = reinterpret_cast<int*>(sbp + A_MISC + 24);
+  // next item: from the shared counter, else a fixed stride over the grid.
+  // The first barrier keeps the write behind every read of the previous
+  // value (an empty item skips the body's barriers).
+  auto next_item = [&](int w) -> int {
+    if (!p.grid_done) return w + gridDim.x;
+    __syncthreads();
+    if (tid == 0) *s_item = atomicAdd(p.grid_done + 1, 1);
+    __syncthreads();
+    return *s_item;
+  };
+  for (int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x); ok && w < p.n_items;
+       w = next_item(w)) {
   const Item cur = item_of(w);
   if (cur.valid <= 0) continue;
   const int h = cur.h, t0 = cur.t0, valid = cur.valid, qrec = cur.qrec;
@@ -822,7 +837,8 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     const int ticket = atomicAdd(p.grid_done, 1);
     if (ticket == (int)(gridDim.x * gridDim.y) - 1) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      *p.grid_done = 0;
+      p.grid_done[0] = 0;
+      p.grid_done[1] = 0;
     }
   }
 }
@@ -1240,16 +1256,17 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   e = device_sms(&sms);
   if (e != cudaSuccess) return e;
 
-  // One CTA per item, two per SM.  dependent: a programmatic dependent launch
-  // of the state pass just enqueued (it may start once that grid's CTAs are
-  // all resident).
-  auto intra = [&](int j_lo, int seg_len, bool dependent) -> cudaError_t {
+  // Two CTAs per SM.  dependent: a programmatic dependent launch of the state
+  // pass just enqueued (it may start once that grid's CTAs are all resident).
+  // persistent: two CTAs per SM take items from a counter, so CTAs that start
+  // late (on SMs a state pass holds) take fewer; else one CTA per item.
+  auto intra = [&](int j_lo, int seg_len, bool dependent, bool persistent) -> cudaError_t {
     const long long items = (long long)pr.n_seq * seg_len * pr.H;
     IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
                    pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items,
-                   dependent ? grid_done : nullptr};
+                   persistent ? grid_done : nullptr};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)items);
+    cfg.gridDim = dim3((unsigned)(persistent ? std::min<long long>(items, 2LL * sms) : items));
     cfg.blockDim = dim3(A_THREADS);
     cfg.dynamicSmemBytes = A_SMEM;
     cfg.stream = stream;
@@ -1286,15 +1303,17 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   const bool overlap = allow_overlap && carry && grid_done &&
                        use_overlap(long_chains, nc_max, sms);
   if (!overlap) {
-    e = intra(0, nc_max, false);
+    const bool persistent = grid_done != nullptr;
+    if (persistent) e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
+    if (e == cudaSuccess) e = intra(0, nc_max, false, persistent);
     if (e == cudaSuccess) e = state(0, nc_max);
     return e;
   }
   const int seg = segment_chunks(nc_max);
-  e = cudaMemsetAsync(grid_done, 0, sizeof(int), stream);
+  e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
   for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
     const int len = std::min(seg, nc_max - j_lo);
-    e = intra(j_lo, len, j_lo > 0);
+    e = intra(j_lo, len, j_lo > 0, true);
     if (e == cudaSuccess) e = state(j_lo, j_lo + len);
   }
   return e;
@@ -1316,7 +1335,7 @@ int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
 namespace {
 
 size_t plan_bytes(int n_seq) { return align_up((size_t)(n_seq + 1) * sizeof(int), 1024); }
-// carried states, then 256 bytes for the finished-CTA counter of the overlapped schedule
+// carried states, then 256 bytes for stage 1's counters (finished CTAs, next item)
 size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float) + 256; }
 
 }  // namespace
