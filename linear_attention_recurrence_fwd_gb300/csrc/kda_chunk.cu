@@ -92,12 +92,16 @@ constexpr uint32_t A_LM = 65536, A_IM = 73728;            // L, I (bf16)      (t
 constexpr uint32_t A_XH = 0;                              // M1 A operand, 64 KB (M1)
 constexpr uint32_t A_KBH = 65536;                         // M1 B operand, 32 KB (M1)
 constexpr uint32_t A_STG = 0;                             // record image [0, 64K) (after M1)
-constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][64]  (after M1)
-constexpr uint32_t A_KT = 81920;                          // (k e^g)^T bf16      (after M1)
-constexpr uint32_t A_WST = 81920;                         // W record image      (after M2)
+constexpr uint32_t A_AKK = 65536;                         // A_kk fp32 [64][AKS] (after M1)
+constexpr uint32_t A_KT = 82944;                          // (k e^g)^T bf16      (after M1)
+constexpr uint32_t A_WST = 82944;                         // W record image      (after M2)
 constexpr uint32_t A_TI = 0;                              // T fp32 (in the W slot, before W)
 constexpr uint32_t A_DINV = 57344;                        // T_aa transposed, 4 KB (in the T diag(beta) slot, before it)
-constexpr uint32_t A_MISC = 98304;                        // barriers, beta, gamma
+constexpr uint32_t A_MISC = 99328;                        // barriers, beta, gamma
+// A_kk row stride in floats: 68 puts the rows' float4 chunks 16 bytes apart
+// in bank order, so 32 rows written at the same column and 8 columns read
+// in one row are both conflict-free.
+constexpr int AKS = 68;
 constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
 // Stage 1 threads: thread t owns key channel (TMEM lane) t % 128 and, in the
 // per-token stages, the token tiles {0, 3} (t < 128) or {1, 2} (t >= 128);
@@ -276,7 +280,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int x = 0; x < 16; ++x) {
-      const float l = akk[(16 * b + x) * CH + 16 * a + rr];
+      const float l = akk[(16 * b + x) * AKS + 16 * a + rr];
       const float4 t = *reinterpret_cast<const float4*>(ti + tix(16 * b + x, 16 * b + 4 * q));
       acc.x += l * t.x;
       acc.y += l * t.y;
@@ -306,7 +310,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     const int cb = tid >> 7, r = 32 + ((tid >> 2) & 31), c0 = 16 * cb + 4 * (tid & 3);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     auto term = [&](int m) {
-      const float l = akk[m * CH + r];
+      const float l = akk[m * AKS + r];
       const float4 t = *reinterpret_cast<const float4*>(ti + tix(m, c0));
       acc.x += l * t.x;
       acc.y += l * t.y;
@@ -617,7 +621,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     }
   }
 
-  // the previous item's last stores read [56K, 64K) and [80K, 96K), which the
+  // the previous item's last stores read [56K, 64K) and [81K, 97K), which the
   // M1 operands (and the ablation's staging) below overwrite
   if (tid == 0) bulk_wait_reads();
   __syncthreads();
@@ -662,13 +666,13 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   const OperandLayout WT = mnmajor(sb + A_WST, 16384);
   if (ok) {
     // ---- A_qk (fp16 record image, MN-major: N = r, K = i) and beta-scaled
-    // strictly-lower A_kk (fp32, stored transposed, akk[i][r] = L[r][i]: the
-    // solve reads L by columns, and an unswizzled row keeps its addresses
-    // compile-time offsets; the stores here conflict, the solve's loads do not).  TMEM lane = key: round 0 (TA_A) lanes 0..63 are the keys
-    // of row tile 3 and lanes 64..111 keys 0..47 of row tile 2; round 1
-    // (TA_G) lanes 0..31 keys of row tile 1 and lanes 32..47 keys 0..15 of
-    // row tile 0.  Columns: q then k rows of the odd tile, then of the even
-    // one.  hh = 0 takes the q columns (A_qk), hh = 1 the k columns (A_kk).
+    // strictly-lower A_kk (fp32, stored transposed, akk[i * AKS + r] =
+    // L[r][i]: the solve reads L by columns).  TMEM lane = key: round 0 (TA_A)
+    // lanes 0..63 are the keys of row tile 3 and lanes 64..111 keys 0..47 of
+    // row tile 2; round 1 (TA_G) lanes 0..31 keys of row tile 1 and lanes
+    // 32..47 keys 0..15 of row tile 0.  Columns: q then k rows of the odd
+    // tile, then of the even one.  hh = 0 takes the q columns (A_qk), hh = 1
+    // the k columns (A_kk).
     auto extract = [&](uint32_t cols, int a, int i) {
       float v[16];
       tmem_ld16(tl + cols + ((a & 1) ? 0 : 32) + 16 * hh, v);
@@ -691,7 +695,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
           x.y = i < r0 + 1 ? s_beta[r0 + 1] * v[q4 + 1] : 0.f;
           x.z = i < r0 + 2 ? s_beta[r0 + 2] * v[q4 + 2] : 0.f;
           x.w = i < r0 + 3 ? s_beta[r0 + 3] * v[q4 + 3] : 0.f;
-          *reinterpret_cast<float4*>(akk + i * CH + r0) = x;
+          *reinterpret_cast<float4*>(akk + i * AKS + r0) = x;
         }
       }
     };
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
           pair_of(pidx, a, rr, ii);
           const int r = 16 * a + rr, i = 16 * a + ii;
           *reinterpret_cast<__half*>(sbp + (layout_addr(AQ, r, i) - sb)) = __float2half_rn(pq[n]);
-          if (ii < rr) akk[i * CH + r] = s_beta[r] * pk[n];
+          if (ii < rr) akk[i * AKS + r] = s_beta[r] * pk[n];
         }
       }
     }
@@ -766,7 +770,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       for (int m = 0; m < 15; ++m) {
         const float xm = x[m];
 #pragma unroll
-        for (int rr = m + 1; rr < 16; ++rr) x[rr] -= akk[(16 * a + m) * CH + 16 * a + rr] * xm;
+        for (int rr = m + 1; rr < 16; ++rr) x[rr] -= akk[(16 * a + m) * AKS + 16 * a + rr] * xm;
       }
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) ti[tix(16 * a + rr, 16 * a + j)] = x[rr];
