@@ -87,7 +87,10 @@ constexpr uint32_t REC_LOAD = 66048;   // bytes copied per record
 constexpr uint32_t REC_BYTES = 66560;  // record stride
 
 // ---- stage 1 shared memory (bytes from a 1024-aligned base); phases reuse space
-constexpr uint32_t A_RQ = 0, A_RK = 16384, A_RG = 32768;  // raw TMA tiles   (transposes)
+// raw TMA tiles (transposes), loaded during the previous item: q and k and
+// the first 64 channels of log alpha where the first record stores read,
+// the other 64 channels of log alpha in a region of their own (A_RG1)
+constexpr uint32_t A_RQ = 16384, A_RK = 32768, A_RG = 49152;
 constexpr uint32_t A_LM = 65536, A_IM = 73728;            // L, I (bf16)      (transposes)
 constexpr uint32_t A_XH = 0;                              // M1 A operand, 64 KB (M1)
 constexpr uint32_t A_KBH = 65536;                         // M1 B operand, 32 KB (M1)
@@ -102,7 +105,9 @@ constexpr uint32_t A_MISC = 99328;                        // barriers, beta, gam
 // in bank order, so 32 rows written at the same column and 8 columns read
 // in one row are both conflict-free.
 constexpr int AKS = 68;
-constexpr uint32_t A_SMEM = A_MISC + 1024 + 1024;         // + alignment slack
+constexpr uint32_t A_RG1 = A_MISC + 1024;                 // raw log alpha, channels 64..127
+constexpr uint32_t A_RG_LBO = A_RG1 - A_RG;               // between the log alpha halves
+constexpr uint32_t A_SMEM = A_RG1 + 8192 + 1024;          // + alignment slack
 // Stage 1 threads: thread t owns key channel (TMEM lane) t % 128 and, in the
 // per-token stages, the token tiles {0, 3} (t < 128) or {1, 2} (t >= 128);
 // that split gives both halves the same share of every M1 version build.
@@ -521,33 +526,49 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     __syncthreads();
     return *s_item;
   };
-  for (int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x); ok && w < p.n_items;
-       w = next_item(w)) {
-  const Item cur = item_of(w);
-  if (cur.valid <= 0) continue;
-  const int h = cur.h, t0 = cur.t0, valid = cur.valid, qrec = cur.qrec;
-  uint8_t* rec = p.records + ((size_t)qrec * H + h) * REC_BYTES;
-
-  if (tid == 0) {
-    // The previous item's stores: all but its last group (W, T diag(beta),
-    // e^{g_C}) are done reading shared memory, and that last group reads
-    // only space this item's loads and L, I do not touch.
-    bulk_wait_reads_but_last();
-    mbar_arrive_expect_tx(bar_tma, 3u * (DIN / 64) * 8192u);
+  // The inputs of item w: thread 0 issues the TMA loads of its q, k and log
+  // alpha tiles, threads below its length load its beta.  Called by all
+  // threads; returns whether loads were issued (the same on every thread).
+  // Each item's loads are issued while the item before it finishes, into
+  // space that item no longer uses.
+  auto prefetch = [&](int w, float& beta_reg) -> bool {
+    beta_reg = 0.f;
+    if (w >= p.n_items) return false;
+    const Item it = item_of(w);
+    if (it.valid <= 0) return false;
+    if (tid < it.valid) beta_reg = __bfloat162float(p.beta[(size_t)(it.t0 + tid) * H + it.h]);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar_tma, 3u * (DIN / 64) * 8192u);
 #pragma unroll
-    for (int b = 0; b < DIN / 64; ++b) {
-      tma_load_3d(sbp + A_RQ + b * 8192, &tm_q, bar_tma, b * 64, h, t0);
-      tma_load_3d(sbp + A_RK + b * 8192, &tm_k, bar_tma, b * 64, h, t0);
-      tma_load_3d(sbp + A_RG + b * 8192, &tm_g, bar_tma, b * 64, h, t0);
+      for (int b = 0; b < DIN / 64; ++b) {
+        tma_load_3d(sbp + A_RQ + b * 8192, &tm_q, bar_tma, b * 64, it.h, it.t0);
+        tma_load_3d(sbp + A_RK + b * 8192, &tm_k, bar_tma, b * 64, it.h, it.t0);
+        tma_load_3d(sbp + A_RG + b * A_RG_LBO, &tm_g, bar_tma, b * 64, it.h, it.t0);
+      }
     }
+    return true;
+  };
+  int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x);
+  float beta_t;
+  bool pending = prefetch(w, beta_t);
+  while (ok && w < p.n_items) {
+  const Item cur = item_of(w);
+  if (cur.valid <= 0) {
+    w = next_item(w);
+    pending = prefetch(w, beta_t);
+    continue;
   }
-  const float beta_t = tid < valid ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-  __syncthreads();
+  const int h = cur.h, valid = cur.valid, qrec = cur.qrec;
+  uint8_t* rec = p.records + ((size_t)qrec * H + h) * REC_BYTES;
+  int w_next = p.n_items;
+  float beta_next = 0.f;
+  bool pending_next = false;
+
   if (DIN == 64) {  // upper channel half of the raw tiles stays zero
     for (uint32_t off = tid * 16; off < 8192; off += A_THREADS * 16) {
       st_shared_v4(sb + A_RQ + 8192 + off, 0, 0, 0, 0);
       st_shared_v4(sb + A_RK + 8192 + off, 0, 0, 0, 0);
-      st_shared_v4(sb + A_RG + 8192 + off, 0, 0, 0, 0);
+      st_shared_v4(sb + A_RG1 + off, 0, 0, 0, 0);
     }
   }
   // L[r][i] = (i <= r), I[r][i] = (i == r), both restricted to valid tokens i
@@ -576,7 +597,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   ok = wait_all(bar_tma, tma_phase);
   if (ok && p.check_decay) {
     bool bad = false;
-    const OperandLayout RG = kmajor(sb + A_RG, 8192);
+    const OperandLayout RG = kmajor(sb + A_RG, A_RG_LBO);
     for (int i = 32 * hh; i < valid && i < 32 * hh + 32; ++i) {
       const float la = bf2f(ld_shared_u16(layout_addr(RG, i, c)));
       bad |= !(la >= -5.f && la <= 0.f);
@@ -587,7 +608,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   if (ok && tid == 0) {
     const uint64_t dq = layout_desc(mnmajor(sb + A_RQ, 8192), 0, 0);
     const uint64_t dk = layout_desc(mnmajor(sb + A_RK, 8192), 0, 0);
-    const uint64_t dg = layout_desc(mnmajor(sb + A_RG, 8192), 0, 0);
+    const uint64_t dg = layout_desc(mnmajor(sb + A_RG, A_RG_LBO), 0, 0);
     const uint64_t dl = layout_desc(LM, 0, 0), di = layout_desc(IM, 0, 0);
 #pragma unroll
     for (int k0 = 0; k0 < CH; k0 += 16) {
@@ -781,6 +802,11 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     __syncthreads();
     // off-diagonal blocks: T_10 and T_32, then the lower-left 32 x 32 block
     solve_offdiag(akk, ti, dinv, tid);
+    // the next item's inputs land where this item's first record stores read
+    // (and in A_RG1): once those reads are done, issue them
+    w_next = next_item(w);
+    if (tid == 0) bulk_wait_reads();
+    pending_next = prefetch(w_next, beta_next);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
     {
       const int r = tid >> 2, i_lo = (tid & 3) * 16;
@@ -828,7 +854,12 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       bulk_commit();
     }
   }
+  w = w_next;
+  beta_t = beta_next;
+  pending = pending_next;
   }  // items
+  // loads still in flight after a failed wait land before the CTA's memory goes away
+  if (pending && tid == 0) mbar_wait(bar_tma, tma_phase);
   if (tid == 0) bulk_wait_all();
   tc_fence_before_sync();
   __syncthreads();
