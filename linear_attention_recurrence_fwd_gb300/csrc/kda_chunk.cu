@@ -1128,6 +1128,9 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     }
     tmem_st_wait();
     bool ok = true;
+    // A checkpoint due before chunk j is stored from the fp32 state that
+    // chunk's decay loads, while the tensor core runs: off the chain.
+    float* ck = nullptr;
     for (int j = 0; j < nchunks; ++j) {
       // invariant: ST = fp16(S_j) written by this thread; TMEM S = S_j
       const int buf = j & 1, ob = j & 1;
@@ -1139,6 +1142,12 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         const float* gam = gamma_of(buf);
         float sv[64];
         tmem_ld64(tl + TB_S + 64 * half, sv);
+        if (ck) {  // S[c][v] = S^T[v][c]
+#pragma unroll
+          for (int c0 = 0; c0 < 64; ++c0)
+            if (c_lo + c0 < DIN) ck[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+          ck = nullptr;
+        }
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) {
           float sd[16];
@@ -1180,10 +1189,14 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         }
         const int done = jb + j + 1;  // chunks of the sequence finished
         if (p.ckpt && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.n_ckpt && v < DIN) {
-          float* ck = p.ckpt + ((size_t)(n * p.n_ckpt + done / p.ckpt_every - 1) * H + h) * DIN * DIN;
+          float* cp = p.ckpt + ((size_t)(n * p.n_ckpt + done / p.ckpt_every - 1) * H + h) * DIN * DIN;
+          if (j + 1 < nchunks) {
+            ck = cp;  // with the next chunk's decay
+          } else {
 #pragma unroll
-          for (int c0 = 0; c0 < 64; ++c0)
-            if (c_lo + c0 < DIN) ck[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+            for (int c0 = 0; c0 < 64; ++c0)
+              if (c_lo + c0 < DIN) cp[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+          }
         }
       }
     }
