@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -104,11 +105,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def source_code(text):
+    """The code of a C/CUDA source: comments, indentation and blank lines
+    removed, so that a comment edit leaves the hash below unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).strip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_hash():
+    """Hash of the prefill kernels' code (not their comments)."""
     h = hashlib.sha256()
     for f in ("kda_chunk.cu", "umma.cuh"):
-        h.update(open(os.path.join(ROOT, "linear_attention_recurrence_fwd_gb300", "csrc", f),
-                      "rb").read())
+        path = os.path.join(ROOT, "linear_attention_recurrence_fwd_gb300", "csrc", f)
+        h.update(source_code(open(path).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,8 +22,9 @@
 // DIAGONAL tiles use the same dense tcgen05 product as the off-diagonal
 // ones; there is no per-position-pair special path.
 //
-// Stage 1 (kda_intra_kernel) needs no state, so it runs one CTA per
-// (chunk, head) over every SM (two CTAs per SM).  It writes a per-chunk
+// Stage 1 (kda_intra_kernel) needs no state, so its (chunk, head) items run
+// on every SM, two CTAs per SM, each loading its next item's inputs while it
+// finishes the current one.  It writes a per-chunk
 // record -- W, q e^g, k e^{g_C - g}, A_qk, T diag(beta) and e^{g_C} -- as
 // byte images of the shared-memory operand tiles stage 2 feeds its MMAs.
 // Stage 2 (kda_state_kernel) walks each (sequence, head) serially,
@@ -439,8 +440,8 @@ template <int DIN, bool PAIRS>
 __global__ void __launch_bounds__(A_THREADS, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
-  // One CTA per item (chunk, head), two CTAs per SM.  The item loop also
-  // covers a grid smaller than the work list.
+  // Two CTAs per SM loop over (chunk, head) items: taken from a counter
+  // (a persistent grid), or without one at a fixed stride over the grid.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int c = tid & (DP - 1), hh = tid >> 7;  // key channel (TMEM lane); token half
