@@ -84,8 +84,11 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
  *                     bytes, 16-byte aligned, owned by the caller; it holds
  *                     the per-(chunk, head) intermediate records (65 KiB
  *                     each) passed from the intra-chunk stage to the state
- *                     pass, and the fp32 state handed between segments of
- *                     the sequence.  Too small or NULL -> KDA_ERR_WORKSPACE.
+ *                     pass, the fp32 state handed between segments of the
+ *                     sequence, and two counters with which the intra-chunk
+ *                     stage hands out its work (so calls sharing a workspace
+ *                     must not overlap on the GPU).  Too small or NULL ->
+ *                     KDA_ERR_WORKSPACE.
  * Long sequences run as segments of chunks, all on `stream`: the
  * intra-chunk stage of one segment is a programmatic dependent launch of
  * the previous segment's state pass and runs on the SMs that pass leaves
