@@ -111,7 +111,7 @@ constexpr uint32_t A_RG_LBO = A_RG1 - A_RG;               // between the log alp
 constexpr uint32_t A_SMEM = A_RG1 + 8192 + 1024;          // + alignment slack
 // Stage 1 threads: thread t owns key channel (TMEM lane) t % 128 and, in the
 // per-token stages, the token tiles {0, 3} (t < 128) or {1, 2} (t >= 128);
-// that split gives both halves the same share of every M1 version build.
+// over the two M1 rounds both halves build nine 16-row operand pieces.
 constexpr int A_THREADS = 256;
 
 // ---- stage 2 shared memory
@@ -122,6 +122,8 @@ constexpr uint32_t B_MISC = 215040;
 constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
+// Stage 1: g, q^T, k^T from the transposes; M1 round 0 in TA_A, round 1 in
+// TA_G (g is consumed by then); W^T from M2 in TA_W.
 constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
 // Stage 2: U~ (M3 result, two buffers), D = [-S^T W^T | -O^T] (two buffers of
 // 128 columns: the U correction and the output share one N = 128 product)
