@@ -111,7 +111,7 @@ constexpr uint32_t A_RG_LBO = A_RG1 - A_RG;               // between the log alp
 constexpr uint32_t A_SMEM = A_RG1 + 8192 + 1024;          // + alignment slack
 // Stage 1 threads: thread t owns key channel (TMEM lane) t % 128 and, in the
 // per-token stages, the token tiles {0, 3} (t < 128) or {1, 2} (t >= 128);
-// over the two M1 rounds both halves build nine 16-row operand pieces.
+// over the two M1 passes both halves build nine 16-row operand pieces.
 constexpr int A_THREADS = 256;
 
 // ---- stage 2 shared memory
@@ -122,7 +122,7 @@ constexpr uint32_t B_MISC = 215040;
 constexpr uint32_t B_SMEM = B_MISC + 1024 + 1024;
 
 // ---- TMEM columns
-// Stage 1: g, q^T, k^T from the transposes; M1 round 0 in TA_A, round 1 in
+// Stage 1: g, q^T, k^T from the transposes; M1 pass 0 in TA_A, pass 1 in
 // TA_G (g is consumed by then); W^T from M2 in TA_W.
 constexpr uint32_t TA_G = 0, TA_Q = 64, TA_K = 128, TA_A = 192, TA_W = 0, TA_COLS = 256;
 // Stage 2: U~ (M3 result, two buffers), D = [-S^T W^T | -O^T] (two buffers of
@@ -218,12 +218,12 @@ __device__ __forceinline__ uint32_t kmaj32_addr(uint32_t cbase, uint32_t cl, int
 // The left factor lies in [e^-80, 1].  The right one lies in [1, e^80] for
 // keys of tile a and is at most 1 for earlier keys, where it may underflow
 // to zero: the exact product is then smaller still.
-//   A operand, M = 128 key rows, K~^(a)_i = k_i e^{R_a - g_i}: round 0 holds
+//   A operand, M = 128 key rows, K~^(a)_i = k_i e^{R_a - g_i}: pass 0 holds
 //     row tile 3's keys 0..63 in rows 0..63 and row tile 2's keys 0..47 in
-//     rows 64..111; round 1 row tile 1's keys 0..31 in rows 0..31 and row
+//     rows 64..111; pass 1 row tile 1's keys 0..31 in rows 0..31 and row
 //     tile 0's keys 0..15 in rows 32..47.
 //   B operand, N = 64 token rows, q_r e^{g_r - R_a} and k_r e^{g_r - R_a}
-//     of the round's row tiles: rows 0..15 / 16..31 q / k of the odd tile
+//     of the pass's row tiles: rows 0..15 / 16..31 q / k of the odd tile
 //     (3 or 1), rows 32..47 / 48..63 q / k of the even tile (2 or 0).
 // A rows left unwritten reach only TMEM lanes that are never read.  The
 // calling thread writes channel c of the rows of its tiles ta[0], ta[1]
@@ -231,16 +231,16 @@ __device__ __forceinline__ uint32_t kmaj32_addr(uint32_t cbase, uint32_t cl, int
 // E: every tile's end; Eo, Ep: the end of tile ta[s] and of the tile before
 // it (0 for tile 0).
 template <int R>
-__device__ __forceinline__ void build_round(uint32_t abase, uint32_t bbase, uint32_t cl,
+__device__ __forceinline__ void build_m1_pass(uint32_t abase, uint32_t bbase, uint32_t cl,
                                             uint32_t tl, const float (&p)[2][16],
                                             const float (&E)[4], const float (&Eo)[2],
                                             const float (&Ep)[2], const int (&ta)[2]) {
-  constexpr int AHI = R == 0 ? 3 : 1, ALO = AHI - 1;  // the round's row tiles
+  constexpr int AHI = R == 0 ? 3 : 1, ALO = AHI - 1;  // the pass's row tiles
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int t = ta[s];
     if (t > AHI) continue;           // warp-uniform
-    const bool rows = t >= ALO;      // t is one of the round's row tiles
+    const bool rows = t >= ALO;      // t is one of the pass's row tiles
     float kv[16], qv[16];
     tmem_ld16(tl + TA_K + 16 * t, kv);
     if (rows) tmem_ld16(tl + TA_Q + 16 * t, qv);
@@ -653,10 +653,10 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   float pq[3], pk[3];
   if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, pq, pk);
 
-  // ---- M1 in two rounds of one kind::tf32 product each, K-major fp32
+  // ---- M1 in two passes of one kind::tf32 product each, K-major fp32
   // operands: A = key rows under the references of two row tiles
   // ([128 keys][128 channels]), B = those tiles' token rows ([64][128]).
-  // Round 0 writes TMEM columns TA_A, round 1 TA_G (g is no longer needed).
+  // Pass 0 writes TMEM columns TA_A, pass 1 TA_G (g is no longer needed).
   OperandLayout XA = kmajor(sb + A_XH, 16384), KBA = kmajor(sb + A_KBH, 8192);
   XA.esize = 4;
   KBA.esize = 4;
@@ -665,13 +665,13 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   const uint32_t abase = sb + A_XH + (uint32_t)(c >> 5) * 16384;
   const uint32_t bbase = sb + A_KBH + (uint32_t)(c >> 5) * 8192;
 #pragma unroll
-  for (int round = 0; round < 2; ++round) {
+  for (int pass = 0; pass < 2; ++pass) {
     if (!ok) break;
-    if (round == 0) build_round<0>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
-    if (round == 1) build_round<1>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
+    if (pass == 0) build_m1_pass<0>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
+    if (pass == 1) build_m1_pass<1>(abase, bbase, cl, tl, pr, E, Eo, Ep, ta);
     operands_ready();
     if (tid == 0) {
-      const uint32_t d = tmem + (round == 0 ? TA_A : TA_G);
+      const uint32_t d = tmem + (pass == 0 ? TA_A : TA_G);
 #pragma unroll
       for (int k0 = 0; k0 < DP; k0 += 8)
         umma_tf32(d, layout_desc(XA, 0, k0), layout_desc(KBA, 0, k0), ID_M1, k0 > 0);
@@ -691,9 +691,9 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   if (ok) {
     // ---- A_qk (fp16 record image, MN-major: N = r, K = i) and beta-scaled
     // strictly-lower A_kk (fp32, stored transposed, akk[i * AKS + r] =
-    // L[r][i]: the solve reads L by columns).  TMEM lane = key: round 0 (TA_A)
+    // L[r][i]: the solve reads L by columns).  TMEM lane = key: pass 0 (TA_A)
     // lanes 0..63 are the keys of row tile 3 and lanes 64..111 keys 0..47 of
-    // row tile 2; round 1 (TA_G) lanes 0..31 keys of row tile 1 and lanes
+    // row tile 2; pass 1 (TA_G) lanes 0..31 keys of row tile 1 and lanes
     // 32..47 keys 0..15 of row tile 0.  Columns: q then k rows of the odd
     // tile, then of the even one.  hh = 0 takes the q columns (A_qk), hh = 1
     // the k columns (A_kk).
