@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
     const __nv_bfloat16* __restrict__ beta, float* __restrict__ state, OutT* __restrict__ out,
     float scale) {
   __shared__ float s_alpha[DK], s_k[DK], s_q[DK];
-  __shared__ float s_part[2][8][HALF];  // [a|b][row group][column]
+  // float4 accesses below: the arrays read or written as float4 are 16-byte aligned
+  __shared__ __align__(16) float s_part[2][8][HALF];  // [a|b][row group][column]
   __shared__ float s_kq[4];
 
   const int tid = threadIdx.x;
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
   __syncthreads();
 
   // 64 columns: finish the reductions over the 8 row groups
-  __shared__ float s_u[HALF];
+  __shared__ __align__(16) float s_u[HALF];
   if (tid < HALF) {
     float at = 0.f, bt = 0.f;
 #pragma unroll
@@ -142,8 +143,9 @@ __global__ void __launch_bounds__(128) decode_tokens_kernel(
   constexpr int KT = 8;
   __shared__ float s_alpha[KT][DK], s_k[KT][DK], s_q[KT][DK];
   __shared__ float s_v[KT][COLS], s_beta[KT], s_kq[KT][4];
-  __shared__ float s_part[2][G][COLS];
-  __shared__ float s_u[COLS];
+  // read and written as float4: 16-byte aligned whatever precedes them
+  __shared__ __align__(16) float s_part[2][G][COLS];
+  __shared__ __align__(16) float s_u[COLS];
 
   const int tid = threadIdx.x;
   const int nh = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
