@@ -139,8 +139,9 @@ __global__ void __launch_bounds__(128) decode_tokens_kernel(
   constexpr int RPT = DK / G;       // rows per thread
   // The tokens' activations are staged KT at a time, all loads issued
   // together, so a pass pays one global-memory latency rather than one per
-  // token.
-  constexpr int KT = 8;
+  // token.  Two at a time keeps the kernel at 124 registers, four CTAs per
+  // SM; eight took 158 (three CTAs) and verify 7 % longer.
+  constexpr int KT = 2;
   __shared__ float s_alpha[KT][DK], s_k[KT][DK], s_q[KT][DK];
   __shared__ float s_v[KT][COLS], s_beta[KT], s_kq[KT][4];
   // read and written as float4: 16-byte aligned whatever precedes them

@@ -25,7 +25,7 @@ def _draft(N, K, H, seed):
     return gen.make_inputs(N, K, H, 128, 128, seed=seed, init_std=0.02)
 
 
-# K = 19 stages the drafted tokens in three passes, the last one ragged
+# K = 19 stages the drafted tokens in several passes, the last one ragged
 @pytest.mark.parametrize("N,K,H,out_dtype", [(5, 4, 3, torch.float32), (8, 7, 2, torch.bfloat16),
                                               (3, 1, 2, torch.float32), (3, 19, 2, torch.float32)])
 def test_verify_matches_oracle_and_leaves_state(N, K, H, out_dtype):
@@ -45,7 +45,7 @@ def test_verify_matches_oracle_and_leaves_state(N, K, H, out_dtype):
 
 
 # counts above K are clamped to K; with K = 13 the accepted counts end inside
-# the first and second staging passes and on their boundary
+# staging passes and on their boundaries
 @pytest.mark.parametrize("K,acc", [(5, [0, 1, 2, 5, 3, 9]), (13, [0, 8, 9, 13, 20, 4])])
 def test_commit_matches_oracle_per_accepted_count(K, acc):
     N, H = 6, 2
