@@ -9,6 +9,8 @@ Three independent fp64 evaluations of the same layer:
 * :func:`kda_recurrence` -- the token-by-token definition, in C (``kda_oracle.c``),
   threaded over (sequence, head, block of value columns).  This is the oracle.
 * :func:`brute_force` -- dense transition matrices multiplied out, for T <= 8.
+* :func:`segmented_forward` -- the sequence cut into segments, each reduced to a
+  (cumulative transition, zero-start state) pair, composed by a prefix scan.
 * :func:`chunked` -- the blockwise (chunked) algebra: intra-chunk pair decays,
   a triangular solve for the delta-rule corrections and a state hand-off
   between chunks.  It follows the chunked evaluation the orkas.ai page
@@ -231,3 +233,76 @@ def chunked(q, k, v, log_alpha, beta, initial_state=None, scale=1.0, chunk=64):
             out[t0:t1, h] = scale * ((qc * np.exp(g)) @ S[h] + A_qk @ U)
             S[h] = np.exp(g[-1])[:, None] * S[h] + (kc * np.exp(g[-1][None, :] - g)).T @ U
     return out, S
+
+
+# ---------------------------------------------------------------------------
+# Sequence split into segments (context parallelism).  The orkas.ai page
+# ("Kimi K3 architecture", section "Die Rechnung landet in der
+# Bereitstellungsinfrastruktur") explains why per-segment states cannot just
+# be added for KDA: every token applies a transition to the state it
+# receives.  Each segment is therefore reduced to two quantities that
+# compose, its cumulative transition and the state it produces from a zero
+# start, and every segment's entry state is rebuilt by a prefix scan over
+# those pairs.  Written here for one sequence ([T, H, d] inputs), in fp64.
+#
+#   S_out = M S_in + Z          (M: [d_k, d_k], Z: [d_k, d_v], per head)
+#   M = prod_t (I - beta_t k_t k_t^T) Diag(alpha_t)     (latest token leftmost)
+#   Z = the segment's final state from S_in = 0
+#   (M1, Z1) then (M2, Z2)  ->  (M2 M1, M2 Z1 + Z2)
+
+
+def segment_transition(k, log_alpha, beta):
+    """Cumulative transition M [H, dk, dk] of one segment ([T, H, dk] k and
+    log_alpha, [T, H] beta), applying the tokens' transitions in order."""
+    k, log_alpha, beta = (_f64(x) for x in (k, log_alpha, beta))
+    T, H, dk = k.shape
+    M = np.broadcast_to(np.eye(dk), (H, dk, dk)).copy()
+    for t in range(T):
+        M = np.exp(log_alpha[t])[:, :, None] * M                       # Diag(alpha_t) M
+        M -= beta[t][:, None, None] * k[t][:, :, None] * np.einsum("hc,hcj->hj", k[t], M)[:, None, :]
+    return M
+
+
+def segment_summary(k, v, log_alpha, beta):
+    """(M, Z) of one segment ([T, H, *] inputs): its cumulative transition and
+    its final state from a zero entering state (the token-by-token recurrence)."""
+    k, v, log_alpha, beta = (_f64(x) for x in (k, v, log_alpha, beta))
+    _, Z = kda_recurrence(np.zeros_like(k)[None], k[None], v[None], log_alpha[None], beta[None])
+    return segment_transition(k, log_alpha, beta), Z[0]
+
+
+def compose_summaries(first, second):
+    """The pair of two consecutive segments, `first` then `second`."""
+    (M1, Z1), (M2, Z2) = first, second
+    return M2 @ M1, M2 @ Z1 + Z2
+
+
+def segment_entry_states(summaries, initial_state):
+    """Exclusive prefix scan: the state entering each segment, and the final
+    state after the last."""
+    S = _f64(initial_state).copy()
+    entries = []
+    for M, Z in summaries:
+        entries.append(S)
+        S = M @ S + Z
+    return entries, S
+
+
+def segmented_forward(q, k, v, log_alpha, beta, initial_state=None, scale=1.0, seg_len=64):
+    """The layer over one sequence split into segments of seg_len tokens: each
+    segment's (M, Z) pair independently, the prefix scan for the entry states,
+    then each segment again from its entry state.  Returns (out [T, H, dv],
+    final [H, dk, dv]); equal to kda_recurrence up to rounding."""
+    q, k, v, log_alpha, beta = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    S0 = np.zeros((H, dk, dv)) if initial_state is None else _f64(initial_state).reshape(H, dk, dv)
+    bounds = [(t0, min(T, t0 + seg_len)) for t0 in range(0, T, seg_len)]
+    summaries = [segment_summary(k[a:b], v[a:b], log_alpha[a:b], beta[a:b]) for a, b in bounds]
+    entries, final = segment_entry_states(summaries, S0)
+    out = np.zeros((T, H, dv))
+    for (a, b), E in zip(bounds, entries):
+        o, _ = kda_recurrence(q[None, a:b], k[None, a:b], v[None, a:b], log_alpha[None, a:b],
+                              beta[None, a:b], E[None], scale)
+        out[a:b] = o[0]
+    return out, final
