@@ -80,3 +80,21 @@ def test_adding_zero_start_states_is_not_the_answer():
     _, scanned = orc.segment_entry_states(s, np.zeros_like(fin[0]))
     assert np.allclose(scanned, fin[0], rtol=1e-12, atol=1e-13)
     assert np.abs(naive - fin[0]).max() > 0.1 * np.abs(fin).max()
+
+
+def test_chunk_transition_from_the_chunked_quantities():
+    """A chunk's transition in the chunked form's terms,
+    M_c = Diag(e^{g_C}) - K_bar^T W  (W = (I + A_kk)^-1 diag(beta) (k e^g),
+    K_bar = k e^{g_C - g}), equals the product of its tokens' transitions."""
+    _, k, _, la, beta, _ = _inputs(64, 2, 16, seed=10)
+    M_tok = orc.segment_transition(k, la, beta)
+    C = 64
+    for h in range(2):
+        kh, bh = k[:, h], beta[:, h]
+        g = np.cumsum(la[:, h], axis=0)
+        decay = np.exp(g[:, None, :] - g[None, :, :])                     # [r, i, c]
+        A_kk = np.tril(bh[:, None] * np.einsum("rc,ic,ric->ri", kh, kh, decay), -1)
+        W = np.linalg.solve(np.eye(C) + A_kk, bh[:, None] * (kh * np.exp(g)))
+        K_bar = kh * np.exp(g[-1][None, :] - g)
+        M_c = np.diag(np.exp(g[-1])) - K_bar.T @ W
+        assert np.allclose(M_c, M_tok[h], rtol=1e-10, atol=1e-12)
