@@ -1372,6 +1372,9 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
 
 }  // namespace
 
+// Counts the long-lived chains as n_seq * H, which is what launch_stages
+// uses for fixed lengths (the only caller); for packed sequences it uses
+// H * ceil(T_total / max_len), which this signature cannot see.
 int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
   int sms = 0;
   if (device_sms(&sms) != cudaSuccess) return -1;
