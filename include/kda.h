@@ -157,9 +157,10 @@ KDA_API int kda_chunk_fwd_launches(int B, int T, int H);
  *     is launched.  Use kda_chunk_fwd with a caller workspace for those.
  *   - All calls share the array.  Calls whose work overlaps on the GPU (two
  *     streams, or two host threads) race on it; serialise them.
- *   - The first call on each device looks up the array's device address
- *     (with that device current).  Make that first call before capturing
- *     any CUDA graph that uses this entry point.
+ *   - Every call looks up the array's device address on the current
+ *     device (a lookup, not an allocation).  The first lookup on a device
+ *     may load the library's device code there, so make the first call on
+ *     each device before any stream capture.
  */
 KDA_API kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
                                            const void* log_alpha, const void* beta,
@@ -180,11 +181,21 @@ KDA_API kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const v
  *   initial_state   : [N, H, d_k, d_v] fp32 or NULL;  final_state likewise
  *   out             : [T_total, H, d_v]
  *   workspace       : at least kda_varlen_fwd_workspace_size() bytes
+ * Each packed sequence is one request with a fixed-size state of its own
+ * (orkas.ai, "Kimi K3 architecture", section "Die Rechnung landet in der
+ * Bereitstellungsinfrastruktur": the cache of a request holds per-token
+ * pages plus one fixed state), so every sequence starts from its own
+ * initial state and ends in its own final state.
  * Chunks start at each sequence's first token; a sequence's last chunk is
  * masked at its end, so no state leaks between sequences.  The chunk list is
  * planned on the device from cu_seqlens (a prefix sum of ceil(len / 64));
- * the call does not synchronise.  A negative length flags
- * KDA_ERR_INVALID_ARG in the device status word.
+ * the call does not synchronise.  The plan clamps every sequence into
+ * [0, T_total) and to max_seqlen tokens, so no kernel reads or writes
+ * outside the caller's buffers whatever cu_seqlens holds; when it had to
+ * clamp (cu[0] != 0, a decreasing offset, an offset past T_total, or a
+ * sequence longer than max_seqlen) it flags KDA_ERR_INVALID_ARG in the
+ * device status word, and the outputs of the clamped sequences are
+ * unspecified.
  */
 KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             const void* log_alpha, const void* beta,
@@ -195,7 +206,7 @@ KDA_API kda_status_t kda_varlen_fwd(const void* q, const void* k, const void* v,
                             float scale, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
-/* (T_total / 64 + N) * H * 66560 + N * H * 65536 + 256, plus 4 (N + 1)
+/* (T_total / 64 + N) * H * 66560 + N * H * 65536 + 256, plus 4 (3 N + 1)
  * bytes rounded up to 1 KiB. */
 KDA_API size_t kda_varlen_fwd_workspace_size(int N, int T_total, int H, int d_k, int d_v);
 

@@ -46,6 +46,15 @@ KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N,
 KDA_API int kda_probe_tma(const void* src, void* out, int T, int H, int d, int h, int t0, int* status,
                   cudaStream_t stream);
 
+/*
+ * Makes a device-side wait run out on purpose: one CTA allocates TMEM, sets
+ * up an mbarrier that nothing arrives on and waits on it with the KDA
+ * kernels' bounded wait, limited to limit_us microseconds (1..100000).  The
+ * wait gives up, *status (device int) is set to 6 (KDA_ERR_TIMEOUT), the
+ * TMEM is freed and the kernel returns.  Returns 0 / 1 / 4 as above.
+ */
+KDA_API int kda_probe_wait_timeout(int limit_us, int* status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

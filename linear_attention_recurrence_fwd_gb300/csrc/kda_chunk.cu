@@ -427,8 +427,7 @@ __device__ __forceinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t t
 struct IntraParams {
   const __nv_bfloat16* beta;
   uint8_t* records;
-  const int* cu;
-  const int* chunk_base;
+  const int* plan;  // packed sequences: see kda_plan_kernel; null for fixed lengths
   int T, n_seq, H;
   int check_decay;
   int j_lo, seg_len, n_items;
@@ -505,10 +504,10 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     const int item_r = w / H;
     const int n = item_r / p.seg_len, jc = p.j_lo + item_r % p.seg_len;
     int seq0, len;
-    if (p.cu) {
-      seq0 = p.cu[n];
-      len = p.cu[n + 1] - seq0;
-      it.qrec = p.chunk_base[n] + jc;
+    if (p.plan) {
+      seq0 = p.plan[p.n_seq + 1 + n];
+      len = p.plan[2 * p.n_seq + 1 + n];
+      it.qrec = p.plan[n] + jc;
     } else {
       seq0 = n * p.T;
       len = p.T;
@@ -890,8 +889,7 @@ struct StateParams {
   float* s1;
   float* carry;  // [n_seq][H][128][128] fp32, or null for a single range
   void* out;
-  const int* cu;
-  const int* chunk_base;
+  const int* plan;  // packed sequences: see kda_plan_kernel; null for fixed lengths
   int T, n_seq, H;
   int j_lo, j_hi;
   float scale;
@@ -935,10 +933,10 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 100);
 
   int tok0, len, base;
-  if (p.cu) {
-    tok0 = p.cu[n];
-    len = p.cu[n + 1] - tok0;
-    base = p.chunk_base[n];
+  if (p.plan) {
+    tok0 = p.plan[p.n_seq + 1 + n];
+    len = p.plan[2 * p.n_seq + 1 + n];
+    base = p.plan[n];
   } else {
     tok0 = n * p.T;
     len = p.T;
@@ -1210,11 +1208,18 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   if (warp == 0) tmem_dealloc(tmem, TB_COLS);
 }
 
-// Packed sequences: chunk_base[n] = sum_{m < n} ceil(len_m / 64), n = 0..N.
-// A negative length, or one above the caller's max_len (the work list is
-// sized by it), is reported as an invalid argument in the status word.
+// Packed sequences: the plan every later kernel reads instead of cu_seqlens,
+//   plan[n]             = sum_{m < n} ceil(len_m / 64)   (n = 0..N, record offsets)
+//   plan[N + 1 + n]     = start_n,   plan[2N + 1 + n] = len_n   (n < N)
+// with each sequence clamped into [0, T_total) and to at most max_len tokens
+// (the work list is sized by max_len), so that no kernel addresses a token
+// or a record outside the caller's buffers whatever cu_seqlens holds.  A
+// sequence that had to be clamped -- cu[0] != 0, a decreasing offset, an
+// offset past T_total, or a length above max_len -- is reported as an
+// invalid argument in the status word.
 __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ cu, int N,
-                                                        int max_len, int* __restrict__ chunk_base) {
+                                                        int max_len, int T_total,
+                                                        int* __restrict__ plan) {
   __shared__ int warp_tot[32];
   __shared__ int carry_s;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -1224,8 +1229,13 @@ __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ 
     const int i = start + tid;
     int cnt = 0;
     if (i < N) {
-      const int len = cu[i + 1] - cu[i];
-      if (len < 0 || len > max_len) set_status(1);
+      const int a = cu[i], b = cu[i + 1];
+      const int s0 = min(max(a, 0), T_total);
+      const int e0 = min(max(b, s0), T_total);
+      const int len = min(e0 - s0, max_len);
+      if ((i == 0 && a != 0) || b < a || b > T_total || b - a > max_len) set_status(1);
+      plan[N + 1 + i] = s0;
+      plan[2 * N + 1 + i] = len;
       cnt = len > 0 ? (len + CH - 1) / CH : 0;
     }
     int x = cnt;  // inclusive warp scan
@@ -1247,7 +1257,7 @@ __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ 
     }
     __syncthreads();
     const int excl = carry_s + (w > 0 ? warp_tot[w - 1] : 0) + x - cnt;
-    if (i <= N) chunk_base[i] = excl;
+    if (i <= N) plan[i] = excl;
     __syncthreads();
     if (tid == 0) carry_s += warp_tot[31];
     __syncthreads();
@@ -1294,7 +1304,7 @@ bool use_overlap(int n_states, int nc_max, int sms) {
 
 template <int DIN, typename OutT>
 cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tg, int* chunk_base,
+                          const CUtensorMap& tv, const CUtensorMap& tg, int* plan,
                           uint8_t* records, float* carry, int* grid_done, int nc_max,
                           bool allow_overlap, cudaStream_t stream) {
   // the shared-memory opt-in is a per-device function attribute; setting it
@@ -1313,7 +1323,7 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // late (on SMs a state pass holds) take fewer; else one CTA per item.
   auto intra = [&](int j_lo, int seg_len, bool dependent, bool persistent) -> cudaError_t {
     const long long items = (long long)pr.n_seq * seg_len * pr.H;
-    IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, pr.cu_seqlens, chunk_base,
+    IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, plan,
                    pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items,
                    persistent ? grid_done : nullptr};
     cudaLaunchConfig_t cfg = {};
@@ -1330,8 +1340,8 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
                             : cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, false>, tq, tk, tg, ip);
   };
   auto state = [&](int j_lo, int j_hi) -> cudaError_t {
-    StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, pr.cu_seqlens,
-                   chunk_base, pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale,
+    StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, plan,
+                   pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale,
                    pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt};
     kda_state_kernel<DIN, OutT>
         <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
@@ -1388,7 +1398,7 @@ int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
 
 namespace {
 
-size_t plan_bytes(int n_seq) { return align_up((size_t)(n_seq + 1) * sizeof(int), 1024); }
+size_t plan_bytes(int n_seq) { return align_up((size_t)(3 * n_seq + 1) * sizeof(int), 1024); }
 // carried states, then 256 bytes for stage 1's counters (finished CTAs, next item)
 size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float) + 256; }
 
@@ -1410,12 +1420,12 @@ namespace {
 
 // records: per-(chunk, head) records; carry: the state between segments (or
 // null, which forces a single segment).
-cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, int* grid_done,
+cudaError_t launch_impl(const ChunkProblem& pr, int* plan, float* carry, int* grid_done,
                         uint8_t* records, bool allow_overlap, cudaStream_t stream) {
   const uint64_t d = (uint64_t)pr.d, H = (uint64_t)pr.H;
   const bool packed = pr.cu_seqlens != nullptr;
   if (packed) {
-    kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, pr.T, chunk_base);
+    kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, pr.T, pr.T_total, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1430,13 +1440,13 @@ cudaError_t launch_impl(const ChunkProblem& pr, int* chunk_base, float* carry, i
       !make_map_3d_bf16(&tg, pr.log_alpha, d, H, rows, d, H * d, 64, 1, 64, sw))
     return cudaErrorInvalidValue;
   if (pr.d == 128)
-    return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
+    return pr.out_f32 ? launch_stages<128, float>(pr, tq, tk, tv, tg, plan, records, carry,
                                                   grid_done, nc_max, allow_overlap, stream)
-                      : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
+                      : launch_stages<128, __nv_bfloat16>(pr, tq, tk, tv, tg, plan, records,
                                                           carry, grid_done, nc_max, allow_overlap, stream);
-  return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, chunk_base, records, carry,
+  return pr.out_f32 ? launch_stages<64, float>(pr, tq, tk, tv, tg, plan, records, carry,
                                                grid_done, nc_max, allow_overlap, stream)
-                    : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, chunk_base, records,
+                    : launch_stages<64, __nv_bfloat16>(pr, tq, tk, tv, tg, plan, records,
                                                        carry, grid_done, nc_max, allow_overlap, stream);
 }
 
@@ -1457,15 +1467,15 @@ cudaError_t copy_initial_state(const ChunkProblem& pr, cudaStream_t stream) {
 cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream_t stream) {
   if (pr.T_total == 0) return copy_initial_state(pr, stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* chunk_base = nullptr;
+  int* plan = nullptr;
   if (pr.cu_seqlens) {
-    chunk_base = reinterpret_cast<int*>(ws);
+    plan = reinterpret_cast<int*>(ws);
     ws += plan_bytes(pr.n_seq);
   }
   float* carry = reinterpret_cast<float*>(ws);
   int* grid_done = reinterpret_cast<int*>(ws + carry_bytes(pr.n_seq, pr.H) - 256);
   ws += carry_bytes(pr.n_seq, pr.H);
-  return launch_impl(pr, chunk_base, carry, grid_done, ws, true, stream);
+  return launch_impl(pr, plan, carry, grid_done, ws, true, stream);
 }
 
 // ---- allocation-free variant --------------------------------------------
@@ -1482,25 +1492,13 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 size_t noalloc_max_records() { return kNoAllocBytes / REC_BYTES; }
 
 cudaError_t launch_chunk_fwd_noalloc(const ChunkProblem& pr, cudaStream_t stream) {
-  // The array's device address, looked up once per device with that device
-  // current (in host code the symbol is only a host-side stand-in).
-  static std::mutex mu;
-  static void* addr[128] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // The array's device address on the current device.  In host code the
+  // symbol is only a host-side stand-in, so the address is looked up with
+  // the device current, on every call: the lookup allocates nothing, and a
+  // fresh lookup stays right after a device reset reloads the module.
+  void* scratch = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  void* scratch;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-      void* ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-      if (e != cudaSuccess) return e;
-      addr[dev] = ptr;
-    }
-    scratch = addr[dev];
-  }
   if (pr.T_total == 0) return copy_initial_state(pr, stream);
   // one segment (no carried state, no internal streams), records only
   return launch_impl(pr, nullptr, nullptr, nullptr, static_cast<uint8_t*>(scratch), false, stream);

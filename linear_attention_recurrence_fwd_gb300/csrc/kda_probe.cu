@@ -111,7 +111,12 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
     umma_commit(&bar);
   }
   const bool ok = mbar_wait(&bar, 0);
-  if (!ok && lane == 0) atomicExch(status, 6);
+  if (!ok) {
+    // the MMAs may still be writing TMEM: give them one more bounded wait
+    // before the columns are freed below
+    if (lane == 0) atomicExch(status, 6);
+    mbar_wait(&bar, 0, 100000000ull);
+  }
   tc_fence_after_sync();
   if (ok) {
     for (int c0 = 0; c0 < p.N; c0 += 16) {
@@ -147,7 +152,10 @@ __global__ void __launch_bounds__(128) probe_tma_kernel(const __grid_constant__ 
       tma_load_3d(base_ptr + b * 8192, &map, &bar, b * 64, h, t0);
   }
   if (!mbar_wait(&bar, 0)) {
+    // the tile may still be landing in this CTA's shared memory: one more
+    // bounded wait before the CTA exits
     if (threadIdx.x == 0) atomicExch(status, 6);
+    mbar_wait(&bar, 0, 100000000ull);
     return;
   }
   // read back through the K-major SW128 layout: row = token, k = channel
@@ -164,7 +172,42 @@ __global__ void __launch_bounds__(128) probe_tma_kernel(const __grid_constant__ 
   }
 }
 
+// A wait that runs out on purpose: TMEM is allocated, an mbarrier is set up
+// that nothing ever arrives on, and every thread waits on it through the
+// same bounded wait the KDA kernels use, with a limit of limit_ns.  The
+// wait gives up, the kernel records KDA_ERR_TIMEOUT (6) in *status, frees
+// its TMEM and returns, leaving the context usable.
+__global__ void __launch_bounds__(128) probe_timeout_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base_s;
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_s, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = tmem_base_s;
+  const bool ok = mbar_wait(&bar, 0, limit_ns);
+  if (!ok && threadIdx.x == 0) atomicExch(status, 6);
+  if (ok && threadIdx.x == 0) atomicExch(status, -1);  // cannot happen: nothing arrives
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 32);
+}
+
 }  // namespace
+
+extern "C" KDA_API int kda_probe_wait_timeout(int limit_us, int* status, cudaStream_t stream) {
+  if (limit_us <= 0 || limit_us > 100000 || !status) return 1;
+  probe_timeout_kernel<<<1, 128, 0, stream>>>((uint64_t)limit_us * 1000ull, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
 
 extern "C" KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N, int K, int NB,
                               int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,

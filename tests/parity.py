@@ -57,12 +57,3 @@ def assert_bf16_output_close(o, o_ref, max_rel=MAX_REL, mean_rel=MEAN_REL, what=
     mean_bound = mean_rel * rms + np.mean(2.0 ** -9 * np.abs(o_ref))
     assert d.mean() <= mean_bound, f"{what}: mean {d.mean() / rms:.3e} rms"
 
-
-def round_like(ref, out):
-    """The oracle rounded to the output's storage type: for bf16 outputs the
-    final rounding is a precision decision both sides take the same way, so
-    the comparison measures the kernel's arithmetic, not the storage format."""
-    ref = _np(ref)
-    if isinstance(out, torch.Tensor) and out.dtype == torch.bfloat16:
-        return torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
-    return ref

@@ -122,3 +122,18 @@ def test_speculative_argument_errors(lib):
     assert v(N=0) == 0 and v(K=0) == 0
     c = lambda acc=F: lib.kda_decode_commit(F, F, F, F, F, F, acc, 2, 3, 2, 128, 128, None)
     assert c(acc=None) == 1
+
+
+# The fixed-scratch entry point holds at most this many (chunk, head) records
+# (the limit include/kda.h documents for kda_chunk_fwd_noalloc).
+NOALLOC_MAX_RECORDS = 1008
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    call = lambda B, T, H: lib.kda_chunk_fwd_noalloc(F, F, F, F, F, None, F, 1, None, B, T, H,
+                                                     128, 128, 1.0, None)
+    # 1 * ceil(4096 / 64) * 32 = 2048 records: refused before any launch
+    assert call(1, 4096, 32) == 7
+    # one record over the limit
+    assert call(1, 64 * (NOALLOC_MAX_RECORDS + 1), 1) == 7
+    assert call(-1, 64, 1) == 1
