@@ -39,6 +39,13 @@
  *     measure what the bound saves.
  *   - Supported head dims: d_k = d_v = 128, and d_k = d_v = 64 (prefill
  *     only).  Others return KDA_ERR_UNSUPPORTED.
+ *   - Range.  The prefill entry points carry the state in fp32 but feed
+ *     it, and the delta-rule corrections u = beta (v - S^T k) of each chunk,
+ *     to the tensor cores as fp16.  State entries and corrections must stay
+ *     below 6e4 in magnitude (values and states of the unit-variance kind
+ *     are ~1); a larger or non-finite one sets KDA_ERR_RANGE in the device
+ *     status word and the results are then unspecified.  Inside that range
+ *     results scale with (v, initial_state) by powers of two.
  *   - Base pointers must be 16-byte aligned (KDA_ERR_ALIGNMENT), except
  *     beta, which needs only its natural 2-byte alignment.
  */
@@ -64,7 +71,8 @@ typedef enum {
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
     KDA_ERR_DECAY_BOUND = 5, /* device found log_alpha outside [-5, 0]            */
     KDA_ERR_TIMEOUT = 6,     /* a device-side wait hit its iteration limit        */
-    KDA_ERR_WORKSPACE = 7    /* workspace missing or smaller than required        */
+    KDA_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required        */
+    KDA_ERR_RANGE = 8        /* a state-pass operand left the fp16 range          */
 } kda_status_t;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
@@ -260,7 +268,9 @@ KDA_API const char* kda_status_string(kda_status_t status);
 
 /*
  * Reads and clears the device status word that kernels set on a decay-bound
- * violation (when checking is on) or on a wait that hit its iteration limit.
+ * violation (when checking is on), on a wait that hit its iteration limit,
+ * on a packed-sequence plan that had to clamp cu_seqlens, or on a state or
+ * corrected value outside the fp16 operand range (KDA_ERR_RANGE).
  * Synchronises `stream`.  Returns KDA_OK when nothing was flagged.
  */
 KDA_API kda_status_t kda_last_device_status(cudaStream_t stream);

@@ -21,6 +21,7 @@ STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
     3: "pointer not 16-byte aligned", 4: "CUDA error", 5: "log_alpha outside [-5, 0]",
     6: "device wait timed out", 7: "workspace too small",
+    8: "state-pass operand outside the fp16 range",
 }
 
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",

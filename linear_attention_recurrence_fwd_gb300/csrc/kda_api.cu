@@ -66,6 +66,7 @@ const char* kda_status_string(kda_status_t s) {
     case KDA_ERR_DECAY_BOUND: return "log_alpha outside [-5, 0]";
     case KDA_ERR_TIMEOUT: return "device wait timed out";
     case KDA_ERR_WORKSPACE: return "workspace too small";
+    case KDA_ERR_RANGE: return "state-pass operand outside the fp16 range";
   }
   return "unknown status";
 }

@@ -904,6 +904,9 @@ struct StateParams {
 // warps because an issuing thread stalls while the tensor core's queue is
 // full.  Hand-offs are mbarriers (bounded waits), never named barriers, so
 // a timeout anywhere unwinds every role.
+// Largest |state| or |u| entry the fp16 operands of the state pass carry
+// (fp16 max 65504); a larger or non-finite entry sets KDA_ERR_RANGE.
+constexpr float kOperandMax = 60000.f;
 constexpr int B_CHAIN = 256;
 constexpr int B_OUTPUT = 128;
 constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
@@ -931,6 +934,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   uint64_t* ut_ready = full + 9;  // chain -> issuer: U^T operand written, state decayed
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 96);
   int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 100);
+  int* s_range = reinterpret_cast<int*>(sbp + B_MISC + 104);
 
   int tok0, len, base;
   if (p.plan) {
@@ -982,6 +986,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     mbar_init(ut_ready, B_CHAIN);
     mbar_fence_init();
     *s_abort = 0;
+    *s_range = 0;
     if (nchunks > 0) issue_loads(0, 0);
     if (nchunks > 1) issue_loads(1, 1);
   }
@@ -1201,10 +1206,23 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         }
       }
     }
-    if (!ok) fail();
+    if (!ok) {
+      fail();
+    } else {
+      // An fp16 operand that overflowed (a state entry or a correction u
+      // beyond the fp16 range) turns into inf / NaN in every later state, so
+      // one check of the range's last state, after the chain, catches it.
+      float sv[64];
+      tmem_ld64(tl + TB_S + 64 * half, sv);
+      bool in_range = true;
+#pragma unroll
+      for (int c0 = 0; c0 < 64; ++c0) in_range &= fabsf(sv[c0]) <= kOperandMax;
+      if (!in_range) *s_range = 1;
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (tid == 0 && *s_range) set_status(8);
   if (warp == 0) tmem_dealloc(tmem, TB_COLS);
 }
 

@@ -60,6 +60,10 @@ CASES = [
     (128, 32, 64, 0, SW64, 0, 0, SW64, 0, 0, None),
     (128, 32, 64, 1, SW64, 0, 1, SW64, 0, 0, None),
     (128, 64, 64, 0, SW128, 0, 0, SW128, 0, 16, 128),
+    # the state pass: N = 192 as three MN-major blocks one LBO apart, K = 128
+    (128, 192, 128, 0, SW128, 0, 1, SW128, 0, 0, None),
+    # the state pass's value term: A MN-major (a raw v tile), B K-major N = 192
+    (128, 192, 64, 1, SW128, 0, 0, SW128, 0, 0, None),
 ]
 
 
@@ -84,6 +88,14 @@ def test_umma_m64_lane_mapping(probe):
         found[m] = lanes
     expected = {m: [32 * (m // 16) + m % 16] for m in range(64)}
     assert found == expected, f"lane mapping: {found}"
+
+
+def test_umma_m64_mn_major_a(probe):
+    """M = 64 with an MN-major A operand (the A_qk image read as A): rows land
+    on lanes 32 (m // 16) + m % 16."""
+    D, exp = _run(probe, 64, 64, 64, 1, SW128, 0, 1, SW128, 0)
+    lanes = [32 * (m // 16) + m % 16 for m in range(64)]
+    assert _close(D[lanes], exp), f"max err {(D[lanes] - exp).abs().max().item():.3e}"
 
 
 @pytest.mark.parametrize("d,t0", [(128, 0), (128, 64), (64, 32)])
