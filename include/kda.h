@@ -115,8 +115,45 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
                            cudaStream_t stream);
 
 /* Bytes of device workspace kda_chunk_fwd needs for this shape:
- * B * ceil(T / 64) * H * 66560 + B * H * 65536 + 256. */
+ * B * ceil(T / 64) * H * 66560 + B * H * 65536 + 256, or, for shapes that
+ * may take the segment scan (ceil(T / 64) >= 2048 and B * H <= 64), that of
+ * kda_chunk_fwd_segments with 8 segments when it is larger. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
+/*
+ * kda_chunk_fwd_segments -- kda_chunk_fwd with each sequence cut into
+ * n_segments segments of whole 64-token chunks that are walked in parallel.
+ * The serial state pass bounds a long sequence with few heads; the orkas.ai
+ * page ("Kimi K3 architecture", section "Die Rechnung landet in der
+ * Bereitstellungsinfrastruktur") splits a sequence by reducing each segment
+ * to a cumulative transition and a zero-start state, which compose, and
+ * rebuilding every segment's entry state with a prefix scan.  Here:
+ *   1. the intra-chunk stage runs once over every chunk;
+ *   2. segment 0 is walked from initial_state with outputs, and every later
+ *      segment q twice at the same time: from zero without values' outputs
+ *      (its zero-start state Z_q) and from the identity without values (its
+ *      transition M_q);
+ *   3. entry states E_1 = state after segment 0, E_{q+1} = M_q E_q + Z_q
+ *      (fp32, one small kernel per (sequence, head));
+ *   4. segments 1.. are walked again from E_q with outputs; the last one
+ *      writes final_state.
+ * n_segments = 1 is kda_chunk_fwd without a scan; larger values are capped
+ * at 8 and at the number of chunks, and reduced so that no segment is
+ * empty.  kda_chunk_fwd takes this path by itself for long sequences with
+ * few (sequence, head) pairs.  Results equal kda_chunk_fwd's up to
+ * rounding (the transitions are carried in fp32 through fp16 operands like
+ * the state).  Arguments and results are those of kda_chunk_fwd; the
+ * workspace is at least kda_chunk_fwd_segments_workspace_size() bytes.
+ */
+KDA_API kda_status_t kda_chunk_fwd_segments(const void* q, const void* k, const void* v,
+                                            const void* log_alpha, const void* beta,
+                                            const float* initial_state, void* out,
+                                            kda_dtype_t out_dtype, float* final_state, int B,
+                                            int T, int H, int d_k, int d_v, float scale,
+                                            int n_segments, void* workspace,
+                                            size_t workspace_bytes, cudaStream_t stream);
+KDA_API size_t kda_chunk_fwd_segments_workspace_size(int B, int T, int H, int d_k, int d_v,
+                                                     int n_segments);
 
 /*
  * kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also saves the recurrent

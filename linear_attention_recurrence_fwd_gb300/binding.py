@@ -25,6 +25,7 @@ STATUS = {
 }
 
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
+           "kda_chunk_fwd_segments", "kda_chunk_fwd_segments_workspace_size",
            "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches", "kda_decode_verify",
            "kda_decode_commit",
            "kda_varlen_fwd",
@@ -58,6 +59,11 @@ def load(path: str = LIB_PATH):
         lib.kda_chunk_fwd_checkpointed.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f] +
                                                    [_vp, _i, _vp, _sz, _vp])
         lib.kda_chunk_fwd_checkpointed.restype = _i
+        lib.kda_chunk_fwd_segments.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _i] +
+                                               [_vp, _sz, _vp])
+        lib.kda_chunk_fwd_segments.restype = _i
+        lib.kda_chunk_fwd_segments_workspace_size.argtypes = [_i] * 6
+        lib.kda_chunk_fwd_segments_workspace_size.restype = _sz
         lib.kda_chunk_fwd_noalloc.argtypes = [_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _vp]
         lib.kda_chunk_fwd_noalloc.restype = _i
         lib.kda_varlen_fwd.argtypes = [_vp] * 6 + [_i, _i, _i, _vp, _vp, _i, _vp, _i, _i, _i, _f,
@@ -150,6 +156,32 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
     _check(lib.kda_chunk_fwd(_p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state),
                              _p(out), _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv,
                              float(scale), _p(ws), ws_bytes, _stream(stream)), "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_segments(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
+                           n_segments=2, out_dtype=torch.float32, out=None, final_state=None,
+                           stream=None):
+    """kda_chunk_fwd with each sequence cut into n_segments segments walked in
+    parallel and joined by a scan of their (transition, zero-start state)
+    pairs.  Returns (out, final_state)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    if initial_state is not None:
+        _need(initial_state, torch.float32, "initial_state")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws_bytes = lib.kda_chunk_fwd_segments_workspace_size(B, T, H, dk, dv, int(n_segments))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    _check(lib.kda_chunk_fwd_segments(
+        _p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state), _p(out),
+        _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv, float(scale), int(n_segments),
+        _p(ws), ws_bytes, _stream(stream)), "kda_chunk_fwd_segments")
     return out, final_state
 
 

@@ -103,6 +103,38 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, const vo
   kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
                       final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(),
                       ablate_diag_env()};
+  p.scan_segs = -1;  // the library decides whether a segment scan pays
+  return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
+}
+
+size_t kda_chunk_fwd_segments_workspace_size(int B, int T, int H, int d_k, int d_v,
+                                             int n_segments) {
+  (void)d_k;
+  (void)d_v;
+  if (B <= 0 || T <= 0 || H <= 0 || n_segments < 1) return 0;
+  return kda::chunk_scan_workspace_bytes(B, T, H, n_segments);
+}
+
+kda_status_t kda_chunk_fwd_segments(const void* q, const void* k, const void* v,
+                                    const void* log_alpha, const void* beta,
+                                    const float* initial_state, void* out, kda_dtype_t out_dtype,
+                                    float* final_state, int B, int T, int H, int d_k, int d_v,
+                                    float scale, int n_segments, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || T < 0 || n_segments < 1) return KDA_ERR_INVALID_ARG;
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, out, out_dtype,
+                                     final_state, H, d_k, d_v, (long long)B * T > 0);
+  if (st != KDA_OK) return st;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
+  if ((long long)B * n_segments > (1 << 20)) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  const size_t need = kda_chunk_fwd_segments_workspace_size(B, T, H, d_k, d_v, n_segments);
+  if (need && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(),
+                      ablate_diag_env()};
+  p.scan_segs = n_segments;
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 

@@ -895,6 +895,16 @@ struct StateParams {
   float scale;
   float* ckpt;  // state after every ckpt_every chunks ([n_seq][n_ckpt][H][d][d]), or null
   int ckpt_every, n_ckpt;
+  // Segment scan (segs > 1): the n_seq sequences of this launch are segments
+  // of segs each of n_seq / segs real sequences (segment p of sequence b is
+  // sequence b * segs + p).  phase 1 walks every segment: segment 0 from the
+  // real initial state with outputs, later segments twice, as the plane
+  // blockIdx.z = 0 from a zero state (their zero-start state Z) and
+  // blockIdx.z = 1 from the identity with no values (their transition M),
+  // both without outputs; every walk leaves its last state in its plane of
+  // carry.  phase 2 walks segments 1.. again with outputs from the entry
+  // states the scan left in carry plane 0, the last one into s1.
+  int segs, phase;
 };
 
 // Stage 2 warp roles: warps 0-7 run the elementwise part of the serial
@@ -911,7 +921,9 @@ constexpr int B_CHAIN = 256;
 constexpr int B_OUTPUT = 128;
 constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
 
-template <int DIN, typename OutT>
+// SCAN: the walks of a segment scan (p.phase 1 or 2); the plain pass is a
+// separate instantiation so that it carries none of that logic.
+template <int DIN, typename OutT, bool SCAN>
 __global__ void __launch_bounds__(B_THREADS, 1)
     kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
   // Every CTA of this grid holds its SM from here on: the next segment's
@@ -949,25 +961,51 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   const int nch_seq = len > 0 ? (len + CH - 1) / CH : 0;
   const int jb = p.j_lo, nchunks = max(0, min(p.j_hi, nch_seq) - jb);  // j below is jb + local
   const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+  // the walk this CTA does: kind 0 the plain recurrence with outputs, 1 the
+  // transition (identity start, no values, no outputs), 2 the zero-start
+  // state (no outputs); and where its first state comes from and its last
+  // state goes
+  const int seg = SCAN ? n % p.segs : 0;
+  const size_t real = (size_t)((SCAN ? n / p.segs : n) * H + h) * DIN * DIN;
+  const size_t plane = (size_t)p.n_seq * H * DIN * DIN;
+  float* carry = p.carry ? p.carry + (SCAN ? blockIdx.z * plane : 0) + sbase : nullptr;
+  int kind = 0;
+  if (SCAN && p.phase == 1 && seg > 0) kind = blockIdx.z ? 1 : 2;
+  if (SCAN && ((p.phase == 1 && seg == 0 && blockIdx.z) || (p.phase == 2 && seg == 0))) return;
+  const bool last_range = jb + nchunks == nch_seq;
+  const float* s_in;
+  float* s_out;
+  if (!SCAN) {
+    s_in = jb == 0 ? (p.s0 ? p.s0 + sbase : nullptr) : carry;
+    s_out = last_range ? (p.s1 ? p.s1 + sbase : nullptr) : carry;
+  } else if (p.phase == 1) {
+    s_in = jb > 0 ? carry : (kind == 0 && p.s0 ? p.s0 + real : nullptr);
+    s_out = carry;
+  } else {
+    s_in = carry;
+    s_out = last_range && seg == p.segs - 1 && p.s1 ? p.s1 + real : nullptr;
+  }
+  const bool ident = SCAN && kind == 1 && jb == 0;  // the transition walk starts from I
+  const bool outputs = !SCAN || kind == 0;
   if (nchunks == 0) {  // nothing in this range; a sequence with no tokens keeps its state
-    if (jb == 0 && nch_seq == 0 && p.s1)
+    if (jb == 0 && nch_seq == 0 && s_out)
       for (int i = threadIdx.x; i < DIN * DIN; i += blockDim.x)
-        p.s1[sbase + i] = p.s0 ? p.s0[sbase + i] : 0.f;
+        s_out[i] = ident ? (i / DIN == i % DIN ? 1.f : 0.f) : (s_in ? s_in[i] : 0.f);
     return;
   }
-  const float* s_in = jb == 0 ? p.s0 : p.carry;
-  float* s_out = jb + nchunks == nch_seq ? p.s1 : p.carry;
   constexpr uint32_t kVBytes = (DIN / 64) * 8192u;
 
   auto issue_loads = [&](int j, int buf) {
     const uint8_t* rec = p.records + ((size_t)(base + jb + j) * H + h) * REC_BYTES;
     uint8_t* dst = sbp + (buf ? B_REC1 : B_REC0);
     uint8_t* vdst = sbp + (buf ? B_V1 : B_V0);
-    mbar_arrive_expect_tx(&full[buf], REC_LOAD + kVBytes);
+    mbar_arrive_expect_tx(&full[buf], REC_LOAD + (SCAN && kind == 1 ? 0u : kVBytes));
     bulk_g2s(dst, rec, REC_LOAD, &full[buf]);
+    if (!SCAN || kind != 1) {
 #pragma unroll
-    for (int b = 0; b < DIN / 64; ++b)
-      tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * (jb + j));
+      for (int b = 0; b < DIN / 64; ++b)
+        tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * (jb + j));
+    }
   };
   auto gamma_of = [&](int buf) {
     return reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
@@ -1023,6 +1061,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is
       // issued as soon as record j lands, ahead of the chain's own products.
       auto issue_m3 = [&](int j) {
+        if (SCAN && kind == 1) return;  // no values: U~ = 0
         const int b = j & 1;
         const uint32_t rb = sb + (b ? B_REC1 : B_REC0), vb = sb + (b ? B_V1 : B_V0);
         const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
@@ -1113,7 +1152,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
                     (size_t)h * DIN + v;
 #pragma unroll
         for (int r = 0; r < CH; ++r)
-          if (r < valid) store_out(out + (size_t)r * H * DIN, -p.scale * o[r]);
+          if (r < valid && (!SCAN || outputs)) store_out(out + (size_t)r * H * DIN, -p.scale * o[r]);
       }
     }
   } else {
@@ -1126,7 +1165,8 @@ __global__ void __launch_bounds__(B_THREADS, 1)
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         const int c = c_lo + c0 + jj;
-        s0[jj] = (s_in && c < DIN && v < DIN) ? s_in[sbase + (size_t)c * DIN + v] : 0.f;
+        s0[jj] = ident ? (c == v && c < DIN ? 1.f : 0.f)
+                       : (s_in && c < DIN && v < DIN) ? s_in[(size_t)c * DIN + v] : 0.f;
       }
       tmem_st16(tl + TB_S + c_lo + c0, s0);
       st8h(layout_addr(ST, v, c_lo + c0), s0);
@@ -1173,8 +1213,13 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         tmem_ld16(tw, *reinterpret_cast<float(*)[16]>(w));
         tmem_ld16(tw + 16, *reinterpret_cast<float(*)[16]>(w + 16));
         tmem_ld_wait();
+        if (SCAN && kind == 1) {  // no values: U = -S W^T alone
 #pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] += w[i];
+          for (int i = 0; i < 32; ++i) u[i] = w[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] += w[i];
+        }
 #pragma unroll
         for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
       }
@@ -1191,7 +1236,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         if (j + 1 == nchunks && s_out && v < DIN) {  // S[c][v] = S^T[v][c]
 #pragma unroll
           for (int c0 = 0; c0 < 64; ++c0)
-            if (c_lo + c0 < DIN) s_out[sbase + (size_t)(c_lo + c0) * DIN + v] = sv[c0];
+            if (c_lo + c0 < DIN) s_out[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
         }
         const int done = jb + j + 1;  // chunks of the sequence finished
         if (p.ckpt && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.n_ckpt && v < DIN) {
@@ -1282,6 +1327,88 @@ __global__ void __launch_bounds__(1024) kda_plan_kernel(const int* __restrict__ 
   }
 }
 
+// Segment scan over fixed-length sequences: segment q of sequence b is
+// sequence b * segs + q of the work list, seg_tok tokens (whole chunks) from
+// token q * seg_tok of sequence b, the last one shorter.  Its records are
+// those of the same chunks of the unsegmented problem.
+__global__ void __launch_bounds__(256) kda_segment_plan_kernel(int B, int T, int seg_tok, int segs,
+                                                               int* __restrict__ plan) {
+  const int N = B * segs, nc = (T + CH - 1) / CH, lc = seg_tok / CH;
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n <= N; n += blockDim.x * gridDim.x) {
+    if (n == N) {
+      plan[N] = B * nc;
+      continue;
+    }
+    const int b = n / segs, q = n % segs;
+    plan[n] = b * nc + q * lc;
+    plan[N + 1 + n] = b * T + q * seg_tok;
+    plan[2 * N + 1 + n] = min(seg_tok, T - q * seg_tok);
+  }
+}
+
+// The scan of a sequence cut into segments (the orkas.ai page, "Kimi K3
+// architecture", section "Die Rechnung landet in der
+// Bereitstellungsinfrastruktur": each segment reduces to a cumulative
+// transition and a zero-start state, composed by a prefix scan).  With M_q,
+// Z_q segment q's transition and zero-start state (planes 1 and 0 of the
+// carried states) and E_1 the state after segment 0 (plane 0 of segment 0),
+//   E_{q+1} = M_q E_q + Z_q,   q = 1 .. segs - 2,
+// in fp32.  E_q replaces Z_q in plane 0, where the second walk of segment q
+// starts from it.  One CTA per (sequence, head).
+template <int DIN>
+constexpr uint32_t kScanSmem = 2u * DIN * (DIN + 4) * 4u;
+
+template <int DIN>
+__global__ void __launch_bounds__(256) kda_scan_combine_kernel(float* __restrict__ carry, int n_seq,
+                                                               int segs, int H) {
+  extern __shared__ float scan_sm[];
+  constexpr int LD = DIN + 4;  // row stride in floats
+  constexpr int TL = DIN / 16;  // each thread: a TL x TL tile of the product
+  float* Ms = scan_sm;
+  float* Cs = scan_sm + DIN * LD;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const size_t mat = (size_t)DIN * DIN, plane = (size_t)n_seq * H * mat;
+  auto at = [&](int z, int q) { return carry + z * plane + ((size_t)(b * segs + q) * H + h) * mat; };
+  const int r0 = (tid / 16) * TL, c0 = (tid % 16) * TL;
+  for (int i = tid; i < DIN * DIN; i += 256) Cs[(i / DIN) * LD + i % DIN] = at(0, 0)[i];
+  __syncthreads();
+  for (int q = 1; q < segs; ++q) {
+    float* Zg = at(0, q);
+    float acc[TL][TL];
+    const bool more = q + 1 < segs;  // E_{q+1} is needed
+    if (more) {
+      const float* Mg = at(1, q);
+      for (int i = tid; i < DIN * DIN; i += 256) Ms[(i / DIN) * LD + i % DIN] = Mg[i];
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < TL; ++i)
+#pragma unroll
+        for (int j = 0; j < TL; ++j) acc[i][j] = Zg[(size_t)(r0 + i) * DIN + c0 + j];
+      for (int k = 0; k < DIN; ++k) {
+        float a[TL], x[TL];
+#pragma unroll
+        for (int i = 0; i < TL; ++i) a[i] = Ms[(r0 + i) * LD + k];
+#pragma unroll
+        for (int j = 0; j < TL; ++j) x[j] = Cs[k * LD + c0 + j];
+#pragma unroll
+        for (int i = 0; i < TL; ++i)
+#pragma unroll
+          for (int j = 0; j < TL; ++j) acc[i][j] = fmaf(a[i], x[j], acc[i][j]);
+      }
+    }
+    __syncthreads();  // every read of Z_q and of E_q in shared memory is done
+    for (int i = tid; i < DIN * DIN; i += 256) Zg[i] = Cs[(i / DIN) * LD + i % DIN];  // E_q
+    __syncthreads();
+    if (more) {
+#pragma unroll
+      for (int i = 0; i < TL; ++i)
+#pragma unroll
+        for (int j = 0; j < TL; ++j) Cs[(r0 + i) * LD + c0 + j] = acc[i][j];
+    }
+    __syncthreads();
+  }
+}
+
 template <typename K>
 cudaError_t set_smem(K kern, uint32_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -1329,7 +1456,8 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // on every call costs next to nothing
   cudaError_t e = set_smem(kda_intra_kernel<DIN, false>, A_SMEM);
   if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, true>, A_SMEM);
-  if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT>, B_SMEM);
+  if (e == cudaSuccess) e = set_smem(kda_state_kernel<DIN, OutT, false>, B_SMEM);
+  if (e == cudaSuccess && pr.scan_segs > 1) e = set_smem(kda_state_kernel<DIN, OutT, true>, B_SMEM);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = device_sms(&sms);
@@ -1357,14 +1485,31 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
     return pr.diag_per_pair ? cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, true>, tq, tk, tg, ip)
                             : cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, false>, tq, tk, tg, ip);
   };
-  auto state = [&](int j_lo, int j_hi) -> cudaError_t {
+  const int segs = pr.scan_segs > 1 ? pr.scan_segs : 1;
+  auto state = [&](int j_lo, int j_hi, int phase) -> cudaError_t {
     StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, plan,
                    pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale,
-                   pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt};
-    kda_state_kernel<DIN, OutT>
-        <<<dim3((unsigned)pr.H, (unsigned)pr.n_seq), B_THREADS, B_SMEM, stream>>>(tv, sp);
+                   pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt, segs, phase};
+    const dim3 grid((unsigned)pr.H, (unsigned)pr.n_seq, phase == 1 ? 2 : 1);
+    if (phase == 0)
+      kda_state_kernel<DIN, OutT, false><<<grid, B_THREADS, B_SMEM, stream>>>(tv, sp);
+    else
+      kda_state_kernel<DIN, OutT, true><<<grid, B_THREADS, B_SMEM, stream>>>(tv, sp);
     return cudaGetLastError();
   };
+  // segment scan, after every segment has been walked: the entry states,
+  // then the later segments once more with outputs
+  auto finish_scan = [&]() -> cudaError_t {
+    if (segs == 1) return cudaSuccess;
+    cudaError_t e2 = set_smem(kda_scan_combine_kernel<DIN>, kScanSmem<DIN>);
+    if (e2 != cudaSuccess) return e2;
+    kda_scan_combine_kernel<DIN><<<dim3((unsigned)pr.H, (unsigned)(pr.n_seq / segs)), 256,
+                                   kScanSmem<DIN>, stream>>>(carry, pr.n_seq, segs, pr.H);
+    e2 = cudaGetLastError();
+    if (e2 == cudaSuccess) e2 = state(0, nc_max, 2);
+    return e2;
+  };
+  const int first_phase = segs > 1 ? 1 : 0;
 
   // Overlapped schedule, all on the caller's stream: segments of chunks,
   //   intra(0), state(0), intra(1)*, state(1), intra(2)*, ...
@@ -1376,16 +1521,19 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // Stage-2 CTAs that stay resident for most of the call: every (sequence,
   // head) for fixed lengths; for packed sequences about H per multiple of the
   // longest length (short sequences' chains end early and give their SMs back).
-  const int long_chains = pr.cu_seqlens
-      ? pr.H * (int)(((long long)pr.T_total + pr.T - 1) / std::max(pr.T, 1))
+  // A segment scan walks 2 segs - 1 chains per (sequence, head); its state
+  // passes are short, so they may take up to every SM.
+  const int long_chains = segs > 1 ? (pr.n_seq / segs) * (2 * segs - 1) * pr.H
+      : pr.cu_seqlens ? pr.H * (int)(((long long)pr.T_total + pr.T - 1) / std::max(pr.T, 1))
       : pr.n_seq * pr.H;
   const bool overlap = allow_overlap && carry && grid_done &&
-                       use_overlap(long_chains, nc_max, sms);
+                       use_overlap(segs > 1 ? long_chains / 2 : long_chains, nc_max, sms);
   if (!overlap) {
     const bool persistent = grid_done != nullptr;
     if (persistent) e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
     if (e == cudaSuccess) e = intra(0, nc_max, false, persistent);
-    if (e == cudaSuccess) e = state(0, nc_max);
+    if (e == cudaSuccess) e = state(0, nc_max, first_phase);
+    if (e == cudaSuccess) e = finish_scan();
     return e;
   }
   const int seg = segment_chunks(nc_max);
@@ -1393,8 +1541,9 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
     const int len = std::min(seg, nc_max - j_lo);
     e = intra(j_lo, len, j_lo > 0, true);
-    if (e == cudaSuccess) e = state(j_lo, j_lo + len);
+    if (e == cudaSuccess) e = state(j_lo, j_lo + len, first_phase);
   }
+  if (e == cudaSuccess) e = finish_scan();
   return e;
 }
 
@@ -1403,22 +1552,60 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
 // Counts the long-lived chains as n_seq * H, which is what launch_stages
 // uses for fixed lengths (the only caller); for packed sequences it uses
 // H * ceil(T_total / max_len), which this signature cannot see.
+// Segments of the scan for B fixed-length sequences of T tokens and H heads
+// (1: no scan).  forced > 0 asks for that many; otherwise the scan is used
+// when the serial chain would bound the call: long sequences (at least
+// kScanMinChunks chunks) and few (sequence, head) chains, with the 2 segs - 1
+// walks per chain fitting on the SMs and segs >= 3 (two segments walk the
+// same number of chunks in a row as none).  Segments are whole chunks and
+// none is empty.
+constexpr int kScanMinChunks = 2048, kScanMaxSegs = 8, kScanMaxChains = 64;
+
+int scan_segments(int B, int T, int H, int sms, int forced) {
+  const int nc = (T + CH - 1) / CH;
+  int segs = forced;
+  if (forced <= 0) {
+    if (nc < kScanMinChunks || (long long)B * H > kScanMaxChains) return 1;
+    segs = std::min(kScanMaxSegs, (sms / (B * H) + 1) / 2);
+    if (segs < 3) return 1;
+  }
+  segs = std::min(std::min(segs, kScanMaxSegs), nc);
+  if (segs <= 1) return 1;
+  const int per = (nc + segs - 1) / segs;  // chunks per segment
+  return (nc + per - 1) / per;
+}
+
 int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
   int sms = 0;
   if (device_sms(&sms) != cudaSuccess) return -1;
-  const int nc_max = (max_len + CH - 1) / CH;
+  int nc_max = (max_len + CH - 1) / CH;
   if (n_seq <= 0 || nc_max <= 0 || H <= 0) return 0;
-  const int plan = packed ? 1 : 0;
-  if (!use_overlap(n_seq * H, nc_max, sms)) return plan + 2;
+  const int segs = packed ? 1 : scan_segments(n_seq, max_len, H, sms, 0);
+  int plan = packed ? 1 : 0, chains = n_seq * H, tail = 0;
+  if (segs > 1) {  // plan, the walks, combine, second walks
+    nc_max = (nc_max + segs - 1) / segs;
+    plan = 1;
+    chains = n_seq * (2 * segs - 1) * H / 2;
+    tail = 2;
+  }
+  if (!use_overlap(chains, nc_max, sms)) return plan + 2 + tail;
   const int seg = segment_chunks(nc_max);
-  return plan + 2 * ((nc_max + seg - 1) / seg);
+  return plan + 2 * ((nc_max + seg - 1) / seg) + tail;
 }
 
 namespace {
 
 size_t plan_bytes(int n_seq) { return align_up((size_t)(3 * n_seq + 1) * sizeof(int), 1024); }
-// carried states, then 256 bytes for stage 1's counters (finished CTAs, next item)
-size_t carry_bytes(int n_seq, int H) { return (size_t)n_seq * H * DP * DP * sizeof(float) + 256; }
+// carried states (planes of them: two for a segment scan), then 256 bytes for
+// stage 1's counters (finished CTAs, next item)
+size_t carry_bytes(int n_seq, int H, int planes = 1) {
+  return (size_t)planes * n_seq * H * DP * DP * sizeof(float) + 256;
+}
+// workspace of a segment scan with segs segments per sequence
+size_t scan_workspace_bytes(int B, long long T, int H, int segs) {
+  const long long chunks = (long long)B * ((T + CH - 1) / CH);
+  return plan_bytes(B * segs) + carry_bytes(B * segs, H, 2) + (size_t)chunks * H * REC_BYTES;
+}
 
 }  // namespace
 
@@ -1431,7 +1618,17 @@ size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H
   } else {
     chunks = (long long)n_seq * ((T_or_total + CH - 1) / CH);
   }
-  return plan + carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
+  size_t bytes = plan + carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
+  // fixed lengths that may take the segment scan: room for its largest form
+  if (!packed && chunks / n_seq >= kScanMinChunks && (long long)n_seq * H <= kScanMaxChains)
+    bytes = std::max(bytes, scan_workspace_bytes(n_seq, T_or_total, H, kScanMaxSegs));
+  return bytes;
+}
+
+size_t chunk_scan_workspace_bytes(int B, long long T, int H, int segs) {
+  if (segs <= 1) return chunk_workspace_bytes(false, B, T, H);
+  const int nc = (int)((T + CH - 1) / CH);
+  return scan_workspace_bytes(B, T, H, std::min(std::min(segs, kScanMaxSegs), nc));
 }
 
 namespace {
@@ -1444,6 +1641,12 @@ cudaError_t launch_impl(const ChunkProblem& pr, int* plan, float* carry, int* gr
   const bool packed = pr.cu_seqlens != nullptr;
   if (packed) {
     kda_plan_kernel<<<1, 1024, 0, stream>>>(pr.cu_seqlens, pr.n_seq, pr.T, pr.T_total, plan);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (pr.scan_segs > 1) {
+    const int B = pr.n_seq / pr.scan_segs;
+    kda_segment_plan_kernel<<<(pr.n_seq + 256) / 256, 256, 0, stream>>>(B, pr.T_total / B, pr.T,
+                                                                        pr.scan_segs, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1482,17 +1685,32 @@ cudaError_t copy_initial_state(const ChunkProblem& pr, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_chunk_fwd(const ChunkProblem& pr, void* workspace, cudaStream_t stream) {
-  if (pr.T_total == 0) return copy_initial_state(pr, stream);
+cudaError_t launch_chunk_fwd(const ChunkProblem& pr_in, void* workspace, cudaStream_t stream) {
+  if (pr_in.T_total == 0) return copy_initial_state(pr_in, stream);
+  ChunkProblem pr = pr_in;
+  int segs = 1;
+  if (!pr.cu_seqlens && pr.scan_segs != 0 && pr.scan_segs != 1) {
+    int sms = 0;
+    cudaError_t e = device_sms(&sms);
+    if (e != cudaSuccess) return e;
+    segs = scan_segments(pr.n_seq, pr.T, pr.H, sms, pr.scan_segs > 0 ? pr.scan_segs : 0);
+  }
+  if (segs > 1) {  // the segments become the sequences of the work list
+    const int nc = (pr.T + CH - 1) / CH, per = (nc + segs - 1) / segs;
+    pr.n_seq *= segs;
+    pr.T = per * CH;
+  }
+  pr.scan_segs = segs;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* plan = nullptr;
-  if (pr.cu_seqlens) {
+  if (pr.cu_seqlens || segs > 1) {
     plan = reinterpret_cast<int*>(ws);
     ws += plan_bytes(pr.n_seq);
   }
+  const int planes = segs > 1 ? 2 : 1;
   float* carry = reinterpret_cast<float*>(ws);
-  int* grid_done = reinterpret_cast<int*>(ws + carry_bytes(pr.n_seq, pr.H) - 256);
-  ws += carry_bytes(pr.n_seq, pr.H);
+  int* grid_done = reinterpret_cast<int*>(ws + carry_bytes(pr.n_seq, pr.H, planes) - 256);
+  ws += carry_bytes(pr.n_seq, pr.H, planes);
   return launch_impl(pr, plan, carry, grid_done, ws, true, stream);
 }
 

@@ -41,11 +41,16 @@ struct ChunkProblem {
   // chunks of a sequence, n_ckpt of them, [n_seq][n_ckpt][H][d][d]
   float* ckpt;
   int ckpt_every_chunks, n_ckpt;
+  // segment scan of fixed-length sequences: -1 lets the library choose, 0
+  // or 1 asks for none, more asks for that many segments of whole chunks
+  int scan_segs;
 };
 
 // Device workspace the chunked prefill needs: per-(chunk, head) records
 // (and, for packed sequences, the per-sequence chunk offsets).
 size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H);
+// The same for B fixed-length sequences cut into segs segments (a scan).
+size_t chunk_scan_workspace_bytes(int B, long long T, int H, int segs);
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 
