@@ -315,6 +315,20 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
     del x, a, o, f
     torch.cuda.empty_cache()
     fixed("long_1m", 3)
+    res["long_1m"]["schedule"] = (f"kda_chunk_fwd chooses the segment scan for this shape "
+                                  f"({binding.kda_chunk_fwd_launches(1, 1 << 20, 16)} launches)")
+    # the same problem with the scan turned off (one segment)
+    w = gen.WORKLOADS["long_1m"]
+    x = gen.workload_inputs(w, device=dev)
+    a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev)
+    f = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    ms = reduce_max(time_call(lambda: binding.kda_chunk_fwd_segments(
+        *a, None, n_segments=1, out=o, final_state=f), 3, 3, stream), ws)
+    res["long_1m_without_scan"] = {"workload": "long_1m through kda_chunk_fwd_segments with "
+                                               "n_segments=1 (one serial state pass per head)",
+                                   "ms": ms, "Mtok_s": ws * w.B * w.T / ms / 1e3, "steps": 3}
+    del x, a, o, f
     torch.cuda.empty_cache()
     return res
 
@@ -322,8 +336,9 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
 def run_profile_case(local):
     """Small, fixed case for ncu captures (a few GB on the device at most):
     two prefills of B=1 T=32768 H=32 (long enough for the overlapped,
-    segmented schedule), two of the 8k workload (plain two-stage schedule)
-    and three decode steps."""
+    segmented schedule), two of the 8k workload (plain two-stage schedule),
+    three decode steps, then one prefill of B=1 T=131072 H=4, which takes
+    the segment scan."""
     from linear_attention_recurrence_fwd_gb300 import binding
     from linear_attention_recurrence_fwd_gb300 import inputs as gen
 
@@ -345,6 +360,10 @@ def run_profile_case(local):
     o = torch.empty((wd.B, wd.H, 128), dtype=torch.float32, device=dev)
     for _ in range(3):
         binding.kda_decode_step(*d, xd["initial_state"], out=o)
+    torch.cuda.synchronize()
+    del xd, d, o
+    x = gen.make_inputs(1, 1 << 17, 4, 128, 128, 3, decay_mean=2.0, device=dev)
+    binding.kda_chunk_fwd(*[x[k] for k in ("q", "k", "v", "log_alpha", "beta")], None)
     torch.cuda.synchronize()
     if binding.kda_last_device_status() != 0:
         raise SystemExit("device status error")
@@ -526,7 +545,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_call,
         "gpu_launches_note": f"{launches_per_call} per prefill call (intra-chunk stage and state "
-                             f"pass, per segment of the overlapped schedule)",
+                             f"pass, per round of the overlapped schedule)",
         "workloads": extra,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -1356,54 +1356,57 @@ __global__ void __launch_bounds__(256) kda_segment_plan_kernel(int B, int T, int
 // in fp32.  E_q replaces Z_q in plane 0, where the second walk of segment q
 // starts from it.  One CTA per (sequence, head).
 template <int DIN>
-constexpr uint32_t kScanSmem = 2u * DIN * (DIN + 4) * 4u;
+constexpr uint32_t kScanSmem = (uint32_t)DIN * (DIN + 4) * 4u + (uint32_t)DIN * (32 + 4) * 4u;
 
+// One CTA per (sequence, head, block of 32 state columns): E's columns are
+// independent under the left multiplication by M.
 template <int DIN>
 __global__ void __launch_bounds__(256) kda_scan_combine_kernel(float* __restrict__ carry, int n_seq,
                                                                int segs, int H) {
   extern __shared__ float scan_sm[];
-  constexpr int LD = DIN + 4;  // row stride in floats
-  constexpr int TL = DIN / 16;  // each thread: a TL x TL tile of the product
-  float* Ms = scan_sm;
-  float* Cs = scan_sm + DIN * LD;
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  constexpr int LD = DIN + 4, LC = 32 + 4;  // row strides in floats
+  constexpr int TR = DIN / 32;              // each thread: TR rows x 4 columns of the product
+  float* Ms = scan_sm;                      // M_q, DIN x DIN
+  float* Cs = scan_sm + DIN * LD;           // E_q, DIN x 32 (this CTA's columns)
+  const int h = blockIdx.x, b = blockIdx.y, col0 = 32 * blockIdx.z, tid = threadIdx.x;
   const size_t mat = (size_t)DIN * DIN, plane = (size_t)n_seq * H * mat;
   auto at = [&](int z, int q) { return carry + z * plane + ((size_t)(b * segs + q) * H + h) * mat; };
-  const int r0 = (tid / 16) * TL, c0 = (tid % 16) * TL;
-  for (int i = tid; i < DIN * DIN; i += 256) Cs[(i / DIN) * LD + i % DIN] = at(0, 0)[i];
+  const int r0 = (tid / 8) * TR, c0 = (tid % 8) * 4;
+  for (int i = tid; i < DIN * 32; i += 256) Cs[(i / 32) * LC + i % 32] = at(0, 0)[(i / 32) * DIN + col0 + i % 32];
   __syncthreads();
   for (int q = 1; q < segs; ++q) {
     float* Zg = at(0, q);
-    float acc[TL][TL];
+    float acc[TR][4];
     const bool more = q + 1 < segs;  // E_{q+1} is needed
     if (more) {
       const float* Mg = at(1, q);
       for (int i = tid; i < DIN * DIN; i += 256) Ms[(i / DIN) * LD + i % DIN] = Mg[i];
       __syncthreads();
 #pragma unroll
-      for (int i = 0; i < TL; ++i)
+      for (int i = 0; i < TR; ++i)
 #pragma unroll
-        for (int j = 0; j < TL; ++j) acc[i][j] = Zg[(size_t)(r0 + i) * DIN + c0 + j];
+        for (int j = 0; j < 4; ++j) acc[i][j] = Zg[(size_t)(r0 + i) * DIN + col0 + c0 + j];
       for (int k = 0; k < DIN; ++k) {
-        float a[TL], x[TL];
+        const float4 x = *reinterpret_cast<const float4*>(Cs + k * LC + c0);
 #pragma unroll
-        for (int i = 0; i < TL; ++i) a[i] = Ms[(r0 + i) * LD + k];
-#pragma unroll
-        for (int j = 0; j < TL; ++j) x[j] = Cs[k * LD + c0 + j];
-#pragma unroll
-        for (int i = 0; i < TL; ++i)
-#pragma unroll
-          for (int j = 0; j < TL; ++j) acc[i][j] = fmaf(a[i], x[j], acc[i][j]);
+        for (int i = 0; i < TR; ++i) {
+          const float a = Ms[(r0 + i) * LD + k];
+          acc[i][0] = fmaf(a, x.x, acc[i][0]);
+          acc[i][1] = fmaf(a, x.y, acc[i][1]);
+          acc[i][2] = fmaf(a, x.z, acc[i][2]);
+          acc[i][3] = fmaf(a, x.w, acc[i][3]);
+        }
       }
     }
-    __syncthreads();  // every read of Z_q and of E_q in shared memory is done
-    for (int i = tid; i < DIN * DIN; i += 256) Zg[i] = Cs[(i / DIN) * LD + i % DIN];  // E_q
+    __syncthreads();  // every read of Z_q's columns and of E_q in shared memory is done
+    for (int i = tid; i < DIN * 32; i += 256)
+      Zg[(size_t)(i / 32) * DIN + col0 + i % 32] = Cs[(i / 32) * LC + i % 32];  // E_q
     __syncthreads();
     if (more) {
 #pragma unroll
-      for (int i = 0; i < TL; ++i)
+      for (int i = 0; i < TR; ++i)
 #pragma unroll
-        for (int j = 0; j < TL; ++j) Cs[(r0 + i) * LD + c0 + j] = acc[i][j];
+        for (int j = 0; j < 4; ++j) Cs[(r0 + i) * LC + c0 + j] = acc[i][j];
     }
     __syncthreads();
   }
@@ -1503,8 +1506,8 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
     if (segs == 1) return cudaSuccess;
     cudaError_t e2 = set_smem(kda_scan_combine_kernel<DIN>, kScanSmem<DIN>);
     if (e2 != cudaSuccess) return e2;
-    kda_scan_combine_kernel<DIN><<<dim3((unsigned)pr.H, (unsigned)(pr.n_seq / segs)), 256,
-                                   kScanSmem<DIN>, stream>>>(carry, pr.n_seq, segs, pr.H);
+    kda_scan_combine_kernel<DIN><<<dim3((unsigned)pr.H, (unsigned)(pr.n_seq / segs), DIN / 32),
+                                   256, kScanSmem<DIN>, stream>>>(carry, pr.n_seq, segs, pr.H);
     e2 = cudaGetLastError();
     if (e2 == cudaSuccess) e2 = state(0, nc_max, 2);
     return e2;
