@@ -306,3 +306,99 @@ def segmented_forward(q, k, v, log_alpha, beta, initial_state=None, scale=1.0, s
                               beta[None, a:b], E[None], scale)
         out[a:b] = o[0]
     return out, final
+
+
+# ---------------------------------------------------------------------------
+# Backward pass (gradients of the layer), for training at 8k and then 64k
+# contexts (the studioglobal.ai page, German edition, section "Große
+# Kapazität ...").  The pages give no algorithm for it; this is the reverse
+# of the token-by-token recurrence above, derived by hand, in fp64:
+#
+#   forward, per token:  S' = Diag(alpha) S_prev,   w = v - S'^T k,
+#                        u = beta w,   S = S' + k u^T,   o = scale S^T q
+#   backward, with G = dL/dS (starting from dL/dS_T) and do = dL/do:
+#     G  += scale q do^T                    (o reads the updated state)
+#     dq  = scale S do
+#     du  = G^T k;     dk = G u;            dv = beta du;   dbeta = <du, w>
+#     dS' = G - beta k du^T;     dk -= beta S' du
+#     dalpha = rowsum(dS' * S_prev);        dlog_alpha = alpha * dalpha
+#     G  <- Diag(alpha) dS'                 (the gradient of S_prev)
+# after the first token, G is the gradient of the initial state.
+
+
+def _loop_states(q, k, v, log_alpha, beta, S0):
+    """Every state of one sequence: S[t] after token t (S[-1]... kept as S0)."""
+    T, H, dk = k.shape
+    states = np.zeros((T + 1,) + S0.shape)
+    states[0] = S0
+    for t in range(T):
+        Sp = np.exp(log_alpha[t])[:, :, None] * states[t]
+        u = beta[t][:, None] * (v[t] - np.einsum("hcv,hc->hv", Sp, k[t]))
+        states[t + 1] = Sp + k[t][:, :, None] * u[:, None, :]
+    return states
+
+
+BWD_MUTATIONS = ("none", "carry_without_decay", "dk_without_correction", "output_after_update",
+                 "dbeta_from_v")
+
+
+def kda_recurrence_bwd(q, k, v, log_alpha, beta, initial_state, d_out, d_final=None,
+                       scale=1.0, cu_seqlens=None, mutation="none"):
+    """Gradients of L = <d_out, out> + <d_final, final_state> for the layer
+    computed by kda_recurrence (same layouts; packed sequences with
+    cu_seqlens).  Returns dict(q, k, v, log_alpha, beta, initial_state) of
+    fp64 arrays shaped like the inputs (initial_state: [N, H, dk, dv]).
+    `mutation` plants a known mistake for the tests that prove the pins catch
+    it ("none" = the derivation above)."""
+    if mutation not in BWD_MUTATIONS:
+        raise ValueError(mutation)
+    q, k, v, log_alpha, beta, d_out = (_f64(x) for x in (q, k, v, log_alpha, beta, d_out))
+    packed = cu_seqlens is not None
+    if packed:
+        if q.ndim == 4:
+            q, k, v, log_alpha, beta, d_out = (x[0] for x in (q, k, v, log_alpha, beta, d_out))
+        cu = [int(c) for c in cu_seqlens]
+    else:
+        B, T = q.shape[:2]
+        cu = [b * T for b in range(B + 1)]
+        q, k, v, log_alpha, beta, d_out = (x.reshape((B * T,) + x.shape[2:]) for x in
+                                           (q, k, v, log_alpha, beta, d_out))
+    N = len(cu) - 1
+    _, H, dk = q.shape
+    dv = v.shape[-1]
+    S0 = (np.zeros((N, H, dk, dv)) if initial_state is None
+          else _f64(initial_state).reshape(N, H, dk, dv))
+    dF = np.zeros((N, H, dk, dv)) if d_final is None else _f64(d_final).reshape(N, H, dk, dv)
+    g = {name: np.zeros_like(x) for name, x in
+         (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta))}
+    g_s0 = np.zeros((N, H, dk, dv))
+    for n in range(N):
+        a, b = cu[n], cu[n + 1]
+        states = _loop_states(q[a:b], k[a:b], v[a:b], log_alpha[a:b], beta[a:b], S0[n])
+        G = dF[n].copy()
+        for t in range(b - a - 1, -1, -1):
+            tt = a + t
+            alpha = np.exp(log_alpha[tt])                               # [H, dk]
+            S_prev, S = states[t], states[t + 1]
+            Sp = alpha[:, :, None] * S_prev
+            w = v[tt] - np.einsum("hcv,hc->hv", Sp, k[tt])             # [H, dv]
+            u = beta[tt][:, None] * w
+            if mutation != "output_after_update":
+                G = G + scale * q[tt][:, :, None] * d_out[tt][:, None, :]
+            g["q"][tt] = scale * np.einsum("hcv,hv->hc", S, d_out[tt])
+            du = np.einsum("hcv,hc->hv", G, k[tt])
+            g["v"][tt] = beta[tt][:, None] * du
+            g["beta"][tt] = np.einsum("hv,hv->h", du, v[tt] if mutation == "dbeta_from_v" else w)
+            dSp = G - beta[tt][:, None, None] * k[tt][:, :, None] * du[:, None, :]
+            g["k"][tt] = np.einsum("hcv,hv->hc", G, u)
+            if mutation != "dk_without_correction":
+                g["k"][tt] -= beta[tt][:, None] * np.einsum("hcv,hv->hc", Sp, du)
+            g["log_alpha"][tt] = alpha * np.einsum("hcv,hcv->hc", dSp, S_prev)
+            G = dSp if mutation == "carry_without_decay" else alpha[:, :, None] * dSp
+            if mutation == "output_after_update":
+                G = G + scale * q[tt][:, :, None] * d_out[tt][:, None, :]
+        g_s0[n] = G
+    if not packed:
+        g = {name: x.reshape((B, T) + x.shape[1:]) for name, x in g.items()}
+    g["initial_state"] = g_s0
+    return g
