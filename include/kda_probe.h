@@ -38,6 +38,18 @@ KDA_API int kda_probe_umma(const void* A, const void* B, float* D, int M, int N,
                    int* status, cudaStream_t stream);
 
 /*
+ * kda_probe_umma with one more switch: a_tmem = 1 writes A (M = 128, bf16,
+ * K <= 128) into tensor memory, row m in lane m, two consecutive K elements
+ * per 32-bit column (the lower half the even one), and runs the MMA with A
+ * read from tensor memory (a_mn must be 0, tf32 0).  a_tmem = 0 is
+ * kda_probe_umma.
+ */
+KDA_API int kda_probe_umma_ta(const void* A, const void* B, float* D, int M, int N, int K, int NB,
+                      int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
+                      int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum, int tf32,
+                      int a_tmem, int* status, cudaStream_t stream);
+
+/*
  * TMA-loads the 64-token x d-channel tile of head h starting at token t0
  * from src (bf16 [T][H][d]) in 64-channel boxes with 128-byte swizzle, and
  * reads it back through the K-major layout function into out (bf16 [64][d]).

@@ -101,6 +101,8 @@ def load_probe(path: str = PROBE_LIB_PATH):
         lib.kda_probe_umma.restype = _i
         lib.kda_probe_tma.argtypes = [_vp, _vp] + [_i] * 5 + [_vp, _vp]
         lib.kda_probe_tma.restype = _i
+        lib.kda_probe_umma_ta.argtypes = [_vp, _vp, _vp] + [_i] * 15 + [_vp, _vp]
+        lib.kda_probe_umma_ta.restype = _i
         lib.kda_probe_wait_timeout.argtypes = [_i, _vp, _vp]
         lib.kda_probe_wait_timeout.restype = _i
         _probe = lib

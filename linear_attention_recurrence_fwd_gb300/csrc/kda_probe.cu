@@ -19,6 +19,7 @@ struct ProbeArgs {
   int b_mn, b_sw, b_mn_blocks_contig;
   int b_row0, neg_a, n_accum;
   int tf32;  // operands are fp32, MMA kind::tf32
+  int a_tmem;  // A is written to tensor memory (bf16 pairs per column) and read from there
 };
 
 constexpr int kProbeSmem = 1024 + 32 * 1024 + 64 * 1024 + 1024;
@@ -86,13 +87,32 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base_s, 256);
+    tmem_alloc(&tmem_base_s, 512);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = tmem_base_s;
+  constexpr uint32_t kATmemCol = 256;
+  if (p.a_tmem) {  // thread (warp, lane) writes row 32 warp + lane of A: K / 2 packed columns
+    const int m = 32 * warp + lane;
+    for (int c0 = 0; c0 < p.K / 2; c0 += 16) {
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int kk = 2 * (c0 + i);
+        const uint32_t lo = m < p.M ? __bfloat16_as_ushort(A[m * p.K + kk]) : 0u;
+        const uint32_t hi = m < p.M ? __bfloat16_as_ushort(A[m * p.K + kk + 1]) : 0u;
+        x[i] = __uint_as_float(lo | (hi << 16));
+      }
+      tmem_st16(tmem_addr(tbase, 32 * warp, kATmemCol + c0), x);
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+  }
 
   if (tid == 0) {
     if (p.tf32) {
@@ -101,6 +121,12 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
         for (int k0 = 0; k0 < p.K; k0 += 8)
           umma_tf32(tbase, layout_desc(LA, 0, k0), layout_desc(LB, p.b_row0, k0), idesc,
                     (rep > 0 || k0 > 0) ? 1u : 0u);
+    } else if (p.a_tmem) {
+      const uint32_t idesc = make_idesc_bf16(p.M, p.N, false, p.b_mn != 0, p.neg_a != 0);
+      for (int rep = 0; rep < p.n_accum; ++rep)
+        for (int k0 = 0; k0 < p.K; k0 += 16)
+          umma_f16_ta(tbase, tbase + kATmemCol + k0 / 2, layout_desc(LB, p.b_row0, k0), idesc,
+                      (rep > 0 || k0 > 0) ? 1u : 0u);
     } else {
       const uint32_t idesc = make_idesc_bf16(p.M, p.N, p.a_mn != 0, p.b_mn != 0, p.neg_a != 0);
       for (int rep = 0; rep < p.n_accum; ++rep)
@@ -129,7 +155,7 @@ __global__ void __launch_bounds__(128) probe_umma_kernel(const __nv_bfloat16* __
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 256);
+  if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 __global__ void __launch_bounds__(128) probe_tma_kernel(const __grid_constant__ CUtensorMap map,
@@ -213,12 +239,23 @@ extern "C" KDA_API int kda_probe_umma(const void* A, const void* B, float* D, in
                               int a_mn, int a_sw, int a_mn_blocks_contig, int b_mn, int b_sw,
                               int b_mn_blocks_contig, int b_row0, int neg_a, int n_accum,
                               int tf32, int* status, cudaStream_t stream) {
+  return kda_probe_umma_ta(A, B, D, M, N, K, NB, a_mn, a_sw, a_mn_blocks_contig, b_mn, b_sw,
+                           b_mn_blocks_contig, b_row0, neg_a, n_accum, tf32, 0, status, stream);
+}
+
+extern "C" KDA_API int kda_probe_umma_ta(const void* A, const void* B, float* D, int M, int N,
+                                         int K, int NB, int a_mn, int a_sw,
+                                         int a_mn_blocks_contig, int b_mn, int b_sw,
+                                         int b_mn_blocks_contig, int b_row0, int neg_a,
+                                         int n_accum, int tf32, int a_tmem, int* status,
+                                         cudaStream_t stream) {
+  if (a_tmem && (M != 128 || tf32 || a_mn || K > 128)) return 1;
   if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K % 16 || K > 128 || K < 16)
     return 1;
   if (NB < b_row0 + N || NB > 256 || (a_mn && M % 64) || n_accum < 1) return 1;
   if (tf32 && (neg_a || (size_t)NB * K * 4 > 64 * 1024 || (size_t)M * K * 4 > 32 * 1024)) return 1;
   ProbeArgs p{M, N, K, NB, a_mn, a_sw, a_mn_blocks_contig, b_mn, b_sw, b_mn_blocks_contig,
-              b_row0, neg_a, n_accum, tf32};
+              b_row0, neg_a, n_accum, tf32, a_tmem};
   if (cudaFuncSetAttribute(probe_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kProbeSmem) != cudaSuccess)
     return 4;

@@ -90,6 +90,26 @@ def test_umma_m64_lane_mapping(probe):
     assert found == expected, f"lane mapping: {found}"
 
 
+@pytest.mark.parametrize("N,K,b_mn", [(64, 64, 0), (128, 128, 1), (192, 128, 1), (128, 64, 0)])
+def test_umma_a_from_tmem(probe, N, K, b_mn):
+    """A read from tensor memory: row m in lane m, two consecutive K elements
+    per 32-bit column, the lower half the even one."""
+    g = torch.Generator().manual_seed(N + K)
+    A = torch.randn(128, K, generator=g).bfloat16()
+    B = torch.randn(N, K, generator=g).bfloat16()
+    Ad, Bd = A.cuda(), B.cuda()  # held: the device copies must outlive the call
+    D = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.kda_probe_umma_ta(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), 128, N, K,
+                                 N, 0, SW128, 0, b_mn, SW128, 0, 0, 0, 1, 0, 1, st.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    exp = A.double() @ B.double().T
+    assert _close(D.cpu().double(), exp), f"max err {(D.cpu().double() - exp).abs().max().item():.3e}"
+
+
 def test_umma_m64_mn_major_a(probe):
     """M = 64 with an MN-major A operand (the A_qk image read as A): rows land
     on lanes 32 (m // 16) + m % 16."""
