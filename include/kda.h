@@ -180,6 +180,44 @@ KDA_API kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, co
                                                 int checkpoint_every, void* workspace,
                                                 size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * kda_chunk_bwd -- backward of kda_chunk_fwd, for training: the gradients of
+ *   L = <d_out, out> + <d_final_state, final_state>
+ * with respect to q, k, v, log_alpha, beta and initial_state.  The pages give
+ * no backward algorithm (the studioglobal.ai page, section "Grosse
+ * Kapazitaet...", names training at 8k and then 64k contexts); this is the
+ * reverse-mode derivative of the token recurrence that kda_chunk_fwd
+ * evaluates, S'_t = Diag(alpha_t) S_{t-1}, u_t = beta_t (v_t - S'_t^T k_t),
+ * S_t = S'_t + k_t u_t^T, o_t = scale S_t^T q_t.
+ *   q, k, v, log_alpha, beta, initial_state, B, T, H, d_k, d_v, scale :
+ *                      the forward's arguments, as in kda_chunk_fwd
+ *   d_out            : [B, T, H, d_v] fp32, 16-byte aligned
+ *   d_final_state    : [B, H, d_k, d_v] fp32, 16-byte aligned, or NULL (zero)
+ *   dq, dk, dlog_alpha: [B, T, H, d_k] fp32, 16-byte aligned
+ *   dv               : [B, T, H, d_v] fp32, 16-byte aligned
+ *   dbeta            : [B, T, H] fp32, 4-byte aligned
+ *   d_initial_state  : [B, H, d_k, d_v] fp32, 16-byte aligned, or NULL (not
+ *                      written)
+ *   workspace        : kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v) bytes,
+ *                      16-byte aligned, owned by the caller; it holds the
+ *                      forward's records, the state at every 64-token
+ *                      boundary and 4 MiB (d = 128) of scratch per sequence
+ *                      and head.
+ * Every gradient buffer is written in full.  The call runs the forward again
+ * (its outputs are not written) and then one CTA per (sequence, head) over
+ * the tokens in reverse, so its time grows with T per sequence and head.
+ * Errors are those of kda_chunk_fwd; a NULL gradient buffer other than
+ * d_initial_state is KDA_ERR_INVALID_ARG.
+ */
+KDA_API kda_status_t kda_chunk_bwd(const void* q, const void* k, const void* v,
+                                   const void* log_alpha, const void* beta,
+                                   const float* initial_state, const float* d_out,
+                                   const float* d_final_state, float* dq, float* dk, float* dv,
+                                   float* dlog_alpha, float* dbeta, float* d_initial_state, int B,
+                                   int T, int H, int d_k, int d_v, float scale, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+KDA_API size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
+
 /* Kernel launches one kda_chunk_fwd call of this shape makes on the current
  * device (the schedule depends on the device's SM count): 2 for the plain
  * two-stage schedule, 2 per segment for the overlapped one.  -1 on a bad

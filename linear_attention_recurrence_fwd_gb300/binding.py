@@ -27,6 +27,7 @@ STATUS = {
 EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noalloc",
            "kda_chunk_fwd_segments", "kda_chunk_fwd_segments_workspace_size",
            "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches", "kda_decode_verify",
+           "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
            "kda_decode_commit",
            "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
@@ -59,6 +60,10 @@ def load(path: str = LIB_PATH):
         lib.kda_chunk_fwd_checkpointed.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f] +
                                                    [_vp, _i, _vp, _sz, _vp])
         lib.kda_chunk_fwd_checkpointed.restype = _i
+        lib.kda_chunk_bwd.argtypes = [_vp] * 14 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+        lib.kda_chunk_bwd.restype = _i
+        lib.kda_chunk_bwd_workspace_size.argtypes = [_i] * 5
+        lib.kda_chunk_bwd_workspace_size.restype = _sz
         lib.kda_chunk_fwd_segments.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f, _i] +
                                                [_vp, _sz, _vp])
         lib.kda_chunk_fwd_segments.restype = _i
@@ -214,6 +219,37 @@ def kda_chunk_fwd_checkpointed(q, k, v, log_alpha, beta, initial_state=None, sca
         _p(checkpoints) if n_ckpt else None, int(checkpoint_every), _p(ws), ws_bytes,
         _stream(stream)), "kda_chunk_fwd_checkpointed")
     return out, final_state, checkpoints
+
+
+def kda_chunk_bwd(q, k, v, log_alpha, beta, d_out, initial_state=None, d_final_state=None,
+                  scale=1.0, want_initial_state_grad=True, stream=None):
+    """Gradients of <d_out, out> + <d_final_state, final_state> for the layer
+    kda_chunk_fwd computes.  Returns a dict of fp32 tensors: q, k, v,
+    log_alpha ([B, T, H, d]), beta ([B, T, H]) and initial_state
+    ([B, H, dk, dv], or None when not asked for)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    _need(d_out, torch.float32, "d_out")
+    for t, n in ((initial_state, "initial_state"), (d_final_state, "d_final_state")):
+        if t is not None:
+            _need(t, torch.float32, n)
+    dev = q.device
+    g = {name: torch.empty((B, T, H, d), dtype=torch.float32, device=dev)
+         for name, d in (("q", dk), ("k", dk), ("v", dv), ("log_alpha", dk))}
+    g["beta"] = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    g["initial_state"] = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+                          if want_initial_state_grad else None)
+    ws_bytes = lib.kda_chunk_bwd_workspace_size(B, T, H, dk, dv)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    _check(lib.kda_chunk_bwd(
+        _p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state), _p(d_out),
+        _p(d_final_state), _p(g["q"]), _p(g["k"]), _p(g["v"]), _p(g["log_alpha"]), _p(g["beta"]),
+        _p(g["initial_state"]), B, T, H, dk, dv, float(scale), _p(ws), ws_bytes,
+        _stream(stream)), "kda_chunk_bwd")
+    return g
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,

@@ -164,6 +164,45 @@ kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
+  if (B <= 0 || T <= 0 || H <= 0 || d_k != d_v || !(d_k == 128 || d_k == 64)) return 0;
+  return kda::chunk_bwd_workspace_bytes(B, T, H, d_k);
+}
+
+kda_status_t kda_chunk_bwd(const void* q, const void* k, const void* v, const void* log_alpha,
+                           const void* beta, const float* initial_state, const float* d_out,
+                           const float* d_final_state, float* dq, float* dk, float* dv,
+                           float* dlog_alpha, float* dbeta, float* d_initial_state, int B, int T,
+                           int H, int d_k, int d_v, float scale, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+  const bool has_tokens = (long long)B * T > 0;
+  // d_out takes the output's place in the forward's checks (fp32, 16-byte aligned)
+  kda_status_t st = validate_prefill(q, k, v, log_alpha, beta, initial_state, d_out, KDA_F32,
+                                     d_final_state, H, d_k, d_v, has_tokens);
+  if (st != KDA_OK) return st;
+  if (has_tokens && (!dq || !dk || !dv || !dlog_alpha || !dbeta)) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dlog_alpha) ||
+      (reinterpret_cast<uintptr_t>(dbeta) & 3u) || (d_initial_state && !aligned16(d_initial_state)))
+    return KDA_ERR_ALIGNMENT;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  if (T == 0) {  // no tokens: the initial state's gradient is the final state's
+    if (!d_initial_state) return KDA_OK;
+    const size_t bytes = (size_t)B * H * d_k * d_v * sizeof(float);
+    return from_cuda(d_final_state ? cudaMemcpyAsync(d_initial_state, d_final_state, bytes,
+                                                     cudaMemcpyDeviceToDevice, stream)
+                                   : cudaMemsetAsync(d_initial_state, 0, bytes, stream));
+  }
+  const size_t need = kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v);
+  if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, nullptr, true,
+                      nullptr, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(), false};
+  return from_cuda(kda::launch_chunk_bwd(p, d_out, d_final_state, dq, dk, dv, dlog_alpha, dbeta,
+                                         d_initial_state, workspace, stream));
+}
+
 kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
                                    const void* log_alpha, const void* beta,
                                    const float* initial_state, void* out, kda_dtype_t out_dtype,

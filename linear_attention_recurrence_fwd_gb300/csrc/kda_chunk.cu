@@ -1147,7 +1147,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
       tmem_ld64(tl + TB_D + 128 * ob + 64, o);  // holds -O^T
       tc_fence_before_sync();
       mbar_arrive(&o_empty[ob]);  // the TMEM tile may be overwritten now
-      if (v < DIN) {
+      if (v < DIN && p.out) {  // (no output buffer: a forward run for its states only)
         OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * (jb + j)) * H * DIN +
                     (size_t)h * DIN + v;
 #pragma unroll

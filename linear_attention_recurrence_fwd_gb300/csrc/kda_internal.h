@@ -54,6 +54,15 @@ size_t chunk_scan_workspace_bytes(int B, long long T, int H, int segs);
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 
+// Backward of the fixed-length prefill described by fwd (its out and
+// final_state are ignored): the forward again for the state at every chunk
+// boundary, then the reverse recurrence.  Gradients are fp32 in the layouts
+// of the inputs; d_final, ds0 may be null.
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d);
+cudaError_t launch_chunk_bwd(const ChunkProblem& fwd, const float* d_out, const float* d_final,
+                             float* dq, float* dk, float* dv, float* dla, float* dbeta, float* ds0,
+                             void* workspace, cudaStream_t stream);
+
 // Kernel launches one prefill call of this shape makes on the current device.
 int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H);
 
