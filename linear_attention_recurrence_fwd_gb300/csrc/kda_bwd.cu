@@ -18,10 +18,11 @@
 // chunks from last to first.  For each chunk it recomputes the 64 token
 // states in fp32 from the saved chunk-start state (S'_t to a per-CTA scratch
 // in global memory, u_t and w_t to shared memory), then runs the reverse
-// recurrence above over the chunk's tokens.  Thread (row c, quarter vg)
-// holds G[c][32 vg .. 32 vg + 31] in registers: dot products along a row
-// take two shuffles, sums down a column (w and du) a warp reduce-scatter and
-// one pass over shared memory.  This is CUDA-core work, serial in tokens per
+// recurrence above over the chunk's tokens.  Thread (row c, vg) holds
+// G[c][4 j + vg] (j < d / 4) in registers, so the four threads of a row read
+// four consecutive words of every shared vector (no bank conflicts): dot
+// products along a row take two shuffles, sums down a column (w and du) a
+// warp reduce-scatter and one pass over shared memory.  This is CUDA-core work, serial in tokens per
 // (sequence, head): a first, exact formulation, not a tensor-core one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,50 +49,48 @@ struct BwdParams {
   float scale;
 };
 
+// One CTA per (sequence, head, block of CB value columns): the columns of G
+// evolve independently (each step scales rows and adds rank-one terms), so
+// only the gradients summed along a row (dq, dk, dlog_alpha, dbeta) combine
+// the blocks, by atomic adds into zeroed buffers.  Thread c owns key row c
+// and the block's CB columns.
+constexpr int CB = 16;
+
 template <int DIN>
 struct BwdShape {
-  static constexpr int THREADS = DIN * 4;   // four threads per key row
-  static constexpr int NV = DIN / 4;        // value columns per thread
+  static constexpr int THREADS = DIN;  // one thread per key row
   static constexpr int WARPS = THREADS / 32;
-  // shared memory: q, k, log alpha, v (bf16), do (fp32), u, w (fp32), the
-  // column-sum partials, one vector, beta
+  static constexpr int BLOCKS = DIN / CB;
+  // shared memory: q, k, log alpha (bf16, every channel), the block's v
+  // (bf16), do, u, w (fp32), the column-sum partials, one vector, beta
   static constexpr size_t OFF_Q = 0;
   static constexpr size_t OFF_K = OFF_Q + BW_CH * DIN * 2;
   static constexpr size_t OFF_LA = OFF_K + BW_CH * DIN * 2;
   static constexpr size_t OFF_V = OFF_LA + BW_CH * DIN * 2;
-  static constexpr size_t OFF_DO = OFF_V + BW_CH * DIN * 2;
-  static constexpr size_t OFF_U = OFF_DO + BW_CH * DIN * 4;
-  static constexpr size_t OFF_W = OFF_U + BW_CH * DIN * 4;
-  static constexpr size_t OFF_RED = OFF_W + BW_CH * DIN * 4;
-  static constexpr size_t OFF_VEC = OFF_RED + WARPS * DIN * 4;
-  static constexpr size_t OFF_BETA = OFF_VEC + DIN * 4;
+  static constexpr size_t OFF_DO = OFF_V + BW_CH * CB * 2;
+  static constexpr size_t OFF_U = OFF_DO + BW_CH * CB * 4;
+  static constexpr size_t OFF_W = OFF_U + BW_CH * CB * 4;
+  static constexpr size_t OFF_RED = OFF_W + BW_CH * CB * 4;
+  static constexpr size_t OFF_VEC = OFF_RED + WARPS * CB * 4;
+  static constexpr size_t OFF_BETA = OFF_VEC + CB * 4;
   static constexpr size_t SMEM = OFF_BETA + BW_CH * 4;
 };
 
-__device__ __forceinline__ float bfv(const __nv_bfloat16* p, int i) {
+__device__ __forceinline__ float bfv(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
 }
 
-// Sum over the four threads of a key row.
-__device__ __forceinline__ float row_sum(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  x += __shfl_xor_sync(0xffffffffu, x, 2);
-  return x;
-}
-
-// Column sums of x (this thread's NV columns of row c) over all DIN rows,
-// left in red[] as per-warp partials: a reduce-scatter over the warp's eight
-// rows (lane bits 2..4) keeps NV / 8 column sums per lane, which it writes
-// to red[warp][column].  The caller synchronises and adds the WARPS
-// partials of each column.
-template <int NV>
-__device__ __forceinline__ void column_partials(float (&x)[NV], float* red, int warp, int lane,
-                                                int vg, int din) {
+// Sum of x over the warp's 32 rows for each of the CB = 16 columns: a
+// reduce-scatter over lane bits 4..1 leaves lanes 2 l and 2 l + 1 with
+// partial sums of column l, which one more exchange adds; lane 2 l writes
+// red[warp][l].  The caller synchronises and adds the warps.
+static_assert(CB == 16, "column_partials is written for 16 columns");
+__device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int warp, int lane) {
 #pragma unroll
-  for (int step = 0; step < 3; ++step) {
-    const int bit = 16 >> step;          // lane bit 4, 3, 2
-    const int half = NV >> (step + 1);   // values kept after this step
-    const bool up = (lane & bit) != 0;   // keep the upper half of the current range
+  for (int step = 0; step < 4; ++step) {
+    const int bit = 16 >> step;         // lane bit 4, 3, 2, 1
+    const int half = CB >> (step + 1);  // values kept after this step
+    const bool up = (lane & bit) != 0;  // keep the upper half of the current range
 #pragma unroll
     for (int i = 0; i < half; ++i) {
       const float send = up ? x[i] : x[i + half];
@@ -100,17 +99,13 @@ __device__ __forceinline__ void column_partials(float (&x)[NV], float* red, int 
       x[i] = keep;
     }
   }
-  // kept range: NV / 8 columns starting at NV/2 b4 + NV/4 b3 + NV/8 b2
-  const int base = ((lane >> 4) & 1) * (NV / 2) + ((lane >> 3) & 1) * (NV / 4) +
-                   ((lane >> 2) & 1) * (NV / 8);
-#pragma unroll
-  for (int i = 0; i < NV / 8; ++i) red[warp * din + NV * vg + base + i] = x[i];
+  x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+  if ((lane & 1) == 0) red[warp * CB + (lane >> 1)] = x[0];  // column 8 b4 + 4 b3 + 2 b2 + b1
 }
 
 template <int DIN>
-__global__ void __launch_bounds__(BwdShape<DIN>::THREADS, 1) kda_bwd_kernel(BwdParams p) {
+__global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdParams p) {
   using S = BwdShape<DIN>;
-  constexpr int NV = S::NV;
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* sq = reinterpret_cast<__nv_bfloat16*>(smem + S::OFF_Q);
   __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(smem + S::OFF_K);
@@ -124,15 +119,28 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS, 1) kda_bwd_kernel(BwdP
   float* sbeta = reinterpret_cast<float*>(smem + S::OFF_BETA);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = tid >> 2, vg = tid & 3, v0 = NV * vg;  // key row, first value column
-  const int h = blockIdx.x, n = blockIdx.y, H = p.H, T = p.T;
+  const int c = tid;  // key row
+  const int h = blockIdx.x, n = blockIdx.y, blk = blockIdx.z, vb = CB * blk;  // first column
+  const int H = p.H, T = p.T;
   const size_t dd = (size_t)DIN * DIN;
-  const size_t plane = ((size_t)n * H + h) * dd;  // this (sequence, head) in [B][H][d][d]
-  float* scratch = p.scratch + ((size_t)n * H + h) * BW_CH * dd;
+  const size_t plane = ((size_t)n * H + h) * dd;     // this (sequence, head) in [B][H][d][d]
+  const size_t row = plane + (size_t)c * DIN + vb;  // element (c, vb)
+  // per-thread scratch of one chunk's S'_t: token i, this thread's CB values
+  float* scratch = p.scratch + (((size_t)n * H + h) * S::BLOCKS + blk) * BW_CH * DIN * CB +
+                   (size_t)tid * CB;
 
-  float g[NV];  // G[c][v0 ..]: the gradient of the state after the current token
+  auto load_row = [&](const float* src, float (&x)[CB]) {  // x = src[c][vb .. vb + CB)
 #pragma unroll
-  for (int j = 0; j < NV; ++j) g[j] = p.dfin ? p.dfin[plane + (size_t)c * DIN + v0 + j] : 0.f;
+    for (int j = 0; j < CB; j += 4) {
+      const float4 f = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[j] = f.x;
+      x[j + 1] = f.y;
+      x[j + 2] = f.z;
+      x[j + 3] = f.w;
+    }
+  };
+  float g[CB];  // G[c][vb ..]: the gradient of the state after the current token
+  load_row(p.dfin ? p.dfin + row : nullptr, g);
 
   const int nch = (T + BW_CH - 1) / BW_CH;
   for (int ch = nch - 1; ch >= 0; --ch) {
@@ -141,131 +149,123 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS, 1) kda_bwd_kernel(BwdP
     __syncthreads();  // the previous chunk is done with shared memory
     for (int e = tid; e < BW_CH * DIN / 8; e += S::THREADS) {  // 8 bf16 (16 bytes) at a time
       const int i = e / (DIN / 8), c8 = (e % (DIN / 8)) * 8;
-      uint4 zq = make_uint4(0, 0, 0, 0), zk = zq, zl = zq, zv = zq;
+      uint4 zq = make_uint4(0, 0, 0, 0), zk = zq, zl = zq;
       if (i < L) {
         const size_t off = (((size_t)n * T + t0 + i) * H + h) * DIN + c8;
         zq = *reinterpret_cast<const uint4*>(p.q + off);
         zk = *reinterpret_cast<const uint4*>(p.k + off);
         zl = *reinterpret_cast<const uint4*>(p.la + off);
-        zv = *reinterpret_cast<const uint4*>(p.v + off);
       }
       *reinterpret_cast<uint4*>(sq + i * DIN + c8) = zq;
       *reinterpret_cast<uint4*>(sk + i * DIN + c8) = zk;
       *reinterpret_cast<uint4*>(sla + i * DIN + c8) = zl;
-      *reinterpret_cast<uint4*>(sv + i * DIN + c8) = zv;
     }
-    for (int e = tid; e < BW_CH * DIN / 4; e += S::THREADS) {  // 4 floats at a time
-      const int i = e / (DIN / 4), c4 = (e % (DIN / 4)) * 4;
+    for (int e = tid; e < BW_CH * CB / 8; e += S::THREADS) {  // the block's v columns
+      const int i = e / (CB / 8), c8 = (e % (CB / 8)) * 8;
+      uint4 z = make_uint4(0, 0, 0, 0);
+      if (i < L) z = *reinterpret_cast<const uint4*>(p.v + (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c8);
+      *reinterpret_cast<uint4*>(sv + i * CB + c8) = z;
+    }
+    for (int e = tid; e < BW_CH * CB / 4; e += S::THREADS) {  // the block's do columns
+      const int i = e / (CB / 4), c4 = (e % (CB / 4)) * 4;
       float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < L) z = *reinterpret_cast<const float4*>(p.dout + (((size_t)n * T + t0 + i) * H + h) * DIN + c4);
-      *reinterpret_cast<float4*>(sdo + i * DIN + c4) = z;
+      if (i < L) z = *reinterpret_cast<const float4*>(p.dout + (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c4);
+      *reinterpret_cast<float4*>(sdo + i * CB + c4) = z;
     }
-    if (tid < BW_CH) sbeta[tid] = tid < L ? bfv(p.beta, (int)(((size_t)n * T + t0 + tid) * H + h)) : 0.f;
+    if (tid < BW_CH) sbeta[tid] = tid < L ? bfv(p.beta, ((size_t)n * T + t0 + tid) * H + h) : 0.f;
     __syncthreads();
 
     // ---- forward over the chunk from its saved starting state
-    float s[NV];
+    float s[CB];
     {
       const float* src = ch == 0 ? (p.s0 ? p.s0 + plane : nullptr)
                                  : p.ckpt + (((size_t)n * p.n_ckpt + (ch - 1)) * H + h) * dd;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) s[j] = src ? src[(size_t)c * DIN + v0 + j] : 0.f;
+      load_row(src ? src + (size_t)c * DIN + vb : nullptr, s);
     }
     for (int i = 0; i < L; ++i) {
       const float a = __expf(__bfloat162float(sla[i * DIN + c]));
       const float kc = __bfloat162float(sk[i * DIN + c]);
-      float x[NV];
+      float x[CB];
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
+      for (int j = 0; j < CB; ++j) {
         s[j] *= a;  // S'_t
         x[j] = s[j] * kc;
       }
-      float* dst = scratch + (size_t)i * dd + (size_t)c * DIN + v0;
+      float* dst = scratch + (size_t)i * DIN * CB;
 #pragma unroll
-      for (int j = 0; j < NV; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-      column_partials<NV>(x, red, warp, lane, vg, DIN);
+      for (int j = 0; j < CB; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+      column_partials(x, red, warp, lane);
       __syncthreads();
-      if (tid < DIN) {  // w = v - S'^T k, u = beta w
+      if (tid < CB) {  // w = v - S'^T k, u = beta w
         float acc = 0.f;
 #pragma unroll
-        for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * DIN + tid];
-        const float w = __bfloat162float(sv[i * DIN + tid]) - acc;
-        sw[i * DIN + tid] = w;
-        su[i * DIN + tid] = sbeta[i] * w;
+        for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * CB + tid];
+        const float w = __bfloat162float(sv[i * CB + tid]) - acc;
+        sw[i * CB + tid] = w;
+        su[i * CB + tid] = sbeta[i] * w;
       }
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < NV; ++j) s[j] += kc * su[i * DIN + v0 + j];  // S_t
+      for (int j = 0; j < CB; ++j) s[j] += kc * su[i * CB + j];  // S_t
     }
 
     // ---- the reverse recurrence over the chunk's tokens
     for (int i = L - 1; i >= 0; --i) {
       const size_t tok = ((size_t)n * T + t0 + i) * H + h;
+      // S'_t, read back from this thread's scratch; the load overlaps the
+      // column sum below, which does not need it
+      float sp[CB];
+      load_row(scratch + (size_t)i * DIN * CB, sp);
       const float qc = __bfloat162float(sq[i * DIN + c]);
       const float kc = __bfloat162float(sk[i * DIN + c]);
       const float a = __expf(__bfloat162float(sla[i * DIN + c]));
       const float b = sbeta[i];
-      const float* dov = sdo + i * DIN + v0;
-      const float* uv = su + i * DIN + v0;
-      float sp[NV];  // S'_t
-      {
-        const float* src = scratch + (size_t)i * dd + (size_t)c * DIN + v0;
+      const float* dov = sdo + i * CB;
+      const float* uv = su + i * CB;
+      // G += scale q do^T, then du = G^T k
+      float x[CB];
 #pragma unroll
-        for (int j = 0; j < NV; j += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(src + j);
-          sp[j] = f.x;
-          sp[j + 1] = f.y;
-          sp[j + 2] = f.z;
-          sp[j + 3] = f.w;
-        }
-      }
-      // G += scale q do^T;  dq = scale S_t do with S_t = S' + k u^T
-      float xq = 0.f;
-      float x[NV];
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const float dov_j = dov[j];
-        g[j] += p.scale * qc * dov_j;
-        xq += (sp[j] + kc * uv[j]) * dov_j;
+      for (int j = 0; j < CB; ++j) {
+        g[j] += p.scale * qc * dov[j];
         x[j] = g[j] * kc;
       }
-      xq = row_sum(xq);
-      if (vg == 0) p.dq[tok * DIN + c] = p.scale * xq;
-      // du = G^T k
-      column_partials<NV>(x, red, warp, lane, vg, DIN);
+      column_partials(x, red, warp, lane);
       __syncthreads();
-      if (tid < DIN) {
-        float acc = 0.f;
+      if (warp == 0) {  // du, dv = beta du, and this block's share of dbeta = du . w
+        float du = 0.f, xb = 0.f;
+        if (lane < CB) {
 #pragma unroll
-        for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * DIN + tid];
-        svec[tid] = acc;
-        p.dv[tok * DIN + tid] = b * acc;
+          for (int wp = 0; wp < S::WARPS; ++wp) du += red[wp * CB + lane];
+          svec[lane] = du;
+          p.dv[tok * DIN + vb + lane] = b * du;
+          xb = du * sw[i * CB + lane];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) xb += __shfl_xor_sync(0xffffffffu, xb, o);
+        if (lane == 0) atomicAdd(p.dbeta + tok, xb);
       }
       __syncthreads();
-      // dk = G u - beta S' du;  dS' = G - beta k du^T;  dlog_alpha = rowsum(dS' o S')
-      float xk = 0.f, xa = 0.f, xb = 0.f;
+      // dq = scale S_t do with S_t = S' + k u^T;  dk = G u - beta S' du;
+      // dS' = G - beta k du^T;  dlog_alpha = rowsum(dS' o S')  (this block's columns)
+      float xq = 0.f, xk = 0.f, xa = 0.f;
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const float du = svec[v0 + j];
-        xk += g[j] * uv[j] - b * sp[j] * du;
+      for (int j = 0; j < CB; ++j) {
+        const float du = svec[j], u = uv[j];
+        xq += (sp[j] + kc * u) * dov[j];
+        xk += g[j] * u - b * sp[j] * du;
         g[j] -= b * kc * du;
         xa += g[j] * sp[j];
-        xb += du * sw[i * DIN + v0 + j];  // the same on every row
         g[j] *= a;  // the gradient of S_{t-1}
       }
-      xk = row_sum(xk);
-      xa = row_sum(xa);
-      xb = row_sum(xb);
-      if (vg == 0) {
-        p.dk[tok * DIN + c] = xk;
-        p.dla[tok * DIN + c] = xa;
-        if (c == 0) p.dbeta[tok] = xb;  // dbeta = du . w
-      }
+      atomicAdd(p.dq + tok * DIN + c, p.scale * xq);
+      atomicAdd(p.dk + tok * DIN + c, xk);
+      atomicAdd(p.dla + tok * DIN + c, xa);
     }
   }
   if (p.ds0) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j) p.ds0[plane + (size_t)c * DIN + v0 + j] = g[j];
+    for (int j = 0; j < CB; j += 4)
+      *reinterpret_cast<float4*>(p.ds0 + row + j) = make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
   }
 }
 
@@ -275,7 +275,7 @@ cudaError_t launch_bwd_kernel(const BwdParams& bp, int B, int H, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_kernel<DIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::SMEM);
   if (e != cudaSuccess) return e;
-  kda_bwd_kernel<DIN><<<dim3((unsigned)H, (unsigned)B), S::THREADS, S::SMEM, stream>>>(bp);
+  kda_bwd_kernel<DIN><<<dim3((unsigned)H, (unsigned)B, S::BLOCKS), S::THREADS, S::SMEM, stream>>>(bp);
   return cudaGetLastError();
 }
 
@@ -317,6 +317,14 @@ cudaError_t launch_chunk_bwd(const ChunkProblem& fwd, const float* d_out, const 
                static_cast<const __nv_bfloat16*>(fwd.v), static_cast<const __nv_bfloat16*>(fwd.log_alpha),
                static_cast<const __nv_bfloat16*>(fwd.beta), fwd.initial_state, ckpt, d_out, d_final,
                dq, dk, dv, dla, dbeta, ds0, scratch, T, H, n_ckpt, fwd.scale};
+  // dq, dk, dlog_alpha and dbeta are summed over the column blocks
+  const size_t tok_bytes = (size_t)B * T * H * d * sizeof(float);
+  for (float* x : {dq, dk, dla}) {
+    e = cudaMemsetAsync(x, 0, tok_bytes, stream);
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaMemsetAsync(dbeta, 0, (size_t)B * T * H * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
   return d == 64 ? launch_bwd_kernel<64>(bp, B, H, stream) : launch_bwd_kernel<128>(bp, B, H, stream);
 }
 
