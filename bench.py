@@ -280,6 +280,21 @@ def extra_workloads(args, ws, dev, stream, x64, ms64):
 
     fixed("prefill_8k", 20)
 
+    # backward of the 8k prefill (training): the forward again for the state
+    # at every chunk boundary, then the reverse token recurrence
+    w = gen.WORKLOADS["prefill_8k"]
+    x = gen.workload_inputs(w, device=dev)
+    a = [x[k] for k in ("q", "k", "v", "log_alpha", "beta")]
+    d_out = torch.randn((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev,
+                        generator=torch.Generator(device=dev).manual_seed(w.seed + 1))
+    ms = reduce_max(time_call(lambda: binding.kda_chunk_bwd(
+        *a, d_out, initial_state=x["initial_state"]), 5, 2, stream), ws)
+    res["backward_8k"] = {"workload": f"gradients of prefill_8k (B={w.B} T={w.T} H={w.H} "
+                                      f"d={w.dk}) for a random d_out, fp32",
+                          "ms": ms, "Mtok_s": ws * w.B * w.T / ms / 1e3,
+                          "forward_ms": res["prefill_8k"]["ms"], "steps": 5}
+    del x, a, d_out
+
     # speculative decoding: verify 4 drafted tokens per sequence (state read
     # once), then commit all 4 (state read and written once)
     wd = gen.WORKLOADS["decode"]

@@ -14,16 +14,16 @@
 //   G    = Diag(alpha_t) dS'                  (gradient of S_{t-1}).
 //
 // Layout of the work: the forward (the chunked tensor-core path) saves the
-// state at every chunk boundary; one CTA per (sequence, head) then walks the
-// chunks from last to first.  For each chunk it recomputes the 64 token
-// states in fp32 from the saved chunk-start state (S'_t to a per-CTA scratch
-// in global memory, u_t and w_t to shared memory), then runs the reverse
-// recurrence above over the chunk's tokens.  Thread (row c, vg) holds
-// G[c][4 j + vg] (j < d / 4) in registers, so the four threads of a row read
-// four consecutive words of every shared vector (no bank conflicts): dot
-// products along a row take two shuffles, sums down a column (w and du) a
-// warp reduce-scatter and one pass over shared memory.  This is CUDA-core work, serial in tokens per
-// (sequence, head): a first, exact formulation, not a tensor-core one.
+// state at every chunk boundary; one CTA per (sequence, head, block of 16
+// value columns) then walks the chunks from last to first.  For each chunk
+// it recomputes the 64 token states in fp32 from the saved chunk-start state
+// (S'_t to a per-CTA scratch in global memory, u_t and w_t to shared
+// memory), then runs the reverse recurrence above over the chunk's tokens.
+// Thread c holds row c of G for the block's columns in registers: dot
+// products along a row stay in the thread, sums down a column (w and du)
+// take a warp reduce-scatter and one pass over shared memory.  This is
+// CUDA-core work, serial in tokens per (sequence, head): a first, exact
+// formulation, not a tensor-core one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
