@@ -431,13 +431,18 @@ struct IntraParams {
   int T, n_seq, H;
   int check_decay;
   int j_lo, seg_len, n_items;
+  // fixed lengths in a ring: the record of chunk j of sequence n is
+  // n * rec_stride + rec_shift + j (as in StateParams)
+  int rec_stride, rec_shift;
   // Overlapped schedule, else null: grid_done[0] counts finished CTAs,
   // grid_done[1] hands out items to a persistent grid.  The CTA that
   // finishes last resets both.
   int* grid_done;
 };
 
-template <int DIN, bool PAIRS>
+// RING: records in a ring (p.rec_stride, p.rec_shift); a separate
+// instantiation, so that the others carry none of it.
+template <int DIN, bool PAIRS, bool RING = false>
 __global__ void __launch_bounds__(A_THREADS, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     } else {
       seq0 = n * p.T;
       len = p.T;
-      it.qrec = n * ((p.T + CH - 1) / CH) + jc;
+      it.qrec = RING ? n * p.rec_stride + p.rec_shift + jc : n * ((p.T + CH - 1) / CH) + jc;
     }
     it.t0 = seq0 + CH * jc;
     it.valid = min(CH, len - CH * jc);
@@ -905,6 +910,10 @@ struct StateParams {
   // carry.  phase 2 walks segments 1.. again with outputs from the entry
   // states the scan left in carry plane 0, the last one into s1.
   int segs, phase;
+  // fixed lengths: the record of chunk j of sequence n is
+  // n * rec_stride + rec_shift + j (one record per chunk, or a ring of two
+  // segments; set by the host per launch)
+  int rec_stride, rec_shift;  // read by the RING instantiation only
 };
 
 // Stage 2 warp roles: warps 0-7 run the elementwise part of the serial
@@ -921,9 +930,10 @@ constexpr int B_CHAIN = 256;
 constexpr int B_OUTPUT = 128;
 constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
 
-// SCAN: the walks of a segment scan (p.phase 1 or 2); the plain pass is a
-// separate instantiation so that it carries none of that logic.
-template <int DIN, typename OutT, bool SCAN>
+// SCAN: the walks of a segment scan (p.phase 1 or 2); RING: records in a
+// ring (p.rec_stride, p.rec_shift).  The plain pass is a separate
+// instantiation so that it carries none of that logic.
+template <int DIN, typename OutT, bool SCAN, bool RING = false>
 __global__ void __launch_bounds__(B_THREADS, 1)
     kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
   // Every CTA of this grid holds its SM from here on: the next segment's
@@ -956,7 +966,7 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   } else {
     tok0 = n * p.T;
     len = p.T;
-    base = n * ((p.T + CH - 1) / CH);
+    base = RING ? n * p.rec_stride + p.rec_shift : n * ((p.T + CH - 1) / CH);
   }
   const int nch_seq = len > 0 ? (len + CH - 1) / CH : 0;
   const int jb = p.j_lo, nchunks = max(0, min(p.j_hi, nch_seq) - jb);  // j below is jb + local
@@ -994,7 +1004,6 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     return;
   }
   constexpr uint32_t kVBytes = (DIN / 64) * 8192u;
-
   auto issue_loads = [&](int j, int buf) {
     const uint8_t* rec = p.records + ((size_t)(base + jb + j) * H + h) * REC_BYTES;
     uint8_t* dst = sbp + (buf ? B_REC1 : B_REC0);
@@ -1443,6 +1452,26 @@ int segment_chunks(int nc_max) {
   return s < 32 ? 32 : (s + 15) / 16 * 16;
 }
 
+// Fixed lengths in the overlapped schedule (no scan) keep the records in a
+// ring of two segments: stage 1 of segment k + 2 starts only after the state
+// pass of segment k has finished (it is a programmatic dependent of the
+// state pass of segment k + 1, which starts after stage 1 of segment k + 1,
+// whose grid completes after the state pass of segment k).  The segment is
+// at most kRingMaxSegment chunks, and less where the ring would exceed
+// kRingBudget, so the workspace stops growing with T.
+constexpr int kRingMaxSegment = 128;
+constexpr size_t kRingBudget = (size_t)1 << 30;
+// The ring is taken only where one record per chunk would pass this size.
+constexpr size_t kRingThreshold = (size_t)4 << 30;
+bool ring_records(int n_seq, int nc, int H) {
+  return (size_t)n_seq * (size_t)nc * (size_t)H * REC_BYTES > kRingThreshold;
+}
+int ring_segment_chunks(int nc_max, int chains) {
+  const long long cap = (long long)(kRingBudget / (2ull * (unsigned)chains * REC_BYTES)) / 16 * 16;
+  const long long seg = std::min<long long>(std::min(segment_chunks(nc_max), kRingMaxSegment), cap);
+  return (int)std::max<long long>(32, seg);
+}
+
 // The overlapped schedule pays off for sequences of at least 128 chunks
 // (8192 tokens) and few long-lived state chains: stage 2 must leave stage 1
 // at least half the SMs.
@@ -1470,10 +1499,12 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // pass just enqueued (it may start once that grid's CTAs are all resident).
   // persistent: two CTAs per SM take items from a counter, so CTAs that start
   // late (on SMs a state pass holds) take fewer; else one CTA per item.
+  int ring = 0;  // records per sequence in a ring (set with the schedule below), 0 = all
   auto intra = [&](int j_lo, int seg_len, bool dependent, bool persistent) -> cudaError_t {
     const long long items = (long long)pr.n_seq * seg_len * pr.H;
     IntraParams ip{static_cast<const __nv_bfloat16*>(pr.beta), records, plan,
                    pr.T, pr.n_seq, pr.H, pr.check_decay ? 1 : 0, j_lo, seg_len, (int)items,
+                   ring ? ring : (pr.T + CH - 1) / CH, ring ? j_lo % ring - j_lo : 0,
                    persistent ? grid_done : nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(persistent ? std::min<long long>(items, 2LL * sms) : items));
@@ -1485,6 +1516,7 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
+    if (ring) return cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, false, true>, tq, tk, tg, ip);
     return pr.diag_per_pair ? cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, true>, tq, tk, tg, ip)
                             : cudaLaunchKernelEx(&cfg, kda_intra_kernel<DIN, false>, tq, tk, tg, ip);
   };
@@ -1492,9 +1524,15 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   auto state = [&](int j_lo, int j_hi, int phase) -> cudaError_t {
     StateParams sp{records, pr.initial_state, pr.final_state, carry, pr.out, plan,
                    pr.T, pr.n_seq, pr.H, j_lo, j_hi, pr.scale,
-                   pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt, segs, phase};
+                   pr.ckpt, pr.ckpt_every_chunks, pr.n_ckpt, segs, phase,
+                   // in a ring, chunk j of this range sits at n ring + j % ring: the
+                   // range is one segment starting at a multiple of its length and the
+                   // ring holds two, so n ring + (j_lo % ring - j_lo) + j stays inside it
+                   ring ? ring : (pr.T + CH - 1) / CH, ring ? j_lo % ring - j_lo : 0};
     const dim3 grid((unsigned)pr.H, (unsigned)pr.n_seq, phase == 1 ? 2 : 1);
-    if (phase == 0)
+    if (phase == 0 && ring)
+      kda_state_kernel<DIN, OutT, false, true><<<grid, B_THREADS, B_SMEM, stream>>>(tv, sp);
+    else if (phase == 0)
       kda_state_kernel<DIN, OutT, false><<<grid, B_THREADS, B_SMEM, stream>>>(tv, sp);
     else
       kda_state_kernel<DIN, OutT, true><<<grid, B_THREADS, B_SMEM, stream>>>(tv, sp);
@@ -1539,7 +1577,14 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
     if (e == cudaSuccess) e = finish_scan();
     return e;
   }
-  const int seg = segment_chunks(nc_max);
+  const bool use_ring = !pr.cu_seqlens && segs == 1 && ring_records(pr.n_seq, nc_max, pr.H);
+  const int seg = use_ring ? ring_segment_chunks(nc_max, long_chains) : segment_chunks(nc_max);
+  if (use_ring) {  // (the per-pair ablation is not offered with a ring)
+    ring = 2 * seg;
+    e = set_smem(kda_state_kernel<DIN, OutT, false, true>, B_SMEM);
+    if (e == cudaSuccess) e = set_smem(kda_intra_kernel<DIN, false, true>, A_SMEM);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
   for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
     const int len = std::min(seg, nc_max - j_lo);
@@ -1592,7 +1637,8 @@ int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
     tail = 2;
   }
   if (!use_overlap(chains, nc_max, sms)) return plan + 2 + tail;
-  const int seg = segment_chunks(nc_max);
+  const int seg = !packed && segs == 1 && ring_records(n_seq, nc_max, H)
+                      ? ring_segment_chunks(nc_max, chains) : segment_chunks(nc_max);
   return plan + 2 * ((nc_max + seg - 1) / seg) + tail;
 }
 
@@ -1613,17 +1659,21 @@ size_t scan_workspace_bytes(int B, long long T, int H, int segs) {
 }  // namespace
 
 size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H) {
-  long long chunks;
-  size_t plan = 0;
-  if (packed) {
-    chunks = T_or_total / CH + n_seq;  // sum of ceil(len / 64) is at most this
-    plan = plan_bytes(n_seq);
-  } else {
-    chunks = (long long)n_seq * ((T_or_total + CH - 1) / CH);
+  if (packed) {  // sum of ceil(len / 64) is at most T_total / 64 + N
+    const long long chunks = T_or_total / CH + n_seq;
+    return plan_bytes(n_seq) + carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
   }
-  size_t bytes = plan + carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
-  // fixed lengths that may take the segment scan: room for its largest form
-  if (!packed && chunks / n_seq >= kScanMinChunks && (long long)n_seq * H <= kScanMaxChains)
+  const long long nc = (T_or_total + CH - 1) / CH;
+  long long chunks = (long long)n_seq * nc;  // one record per chunk
+  // the overlapped schedule keeps the records in a ring of two segments
+  int sms = 0;
+  if (ring_records(n_seq, (int)nc, H) && device_sms(&sms) == cudaSuccess &&
+      use_overlap(n_seq * H, (int)nc, sms))
+    chunks = std::min(chunks, (long long)n_seq * 2 * ring_segment_chunks((int)nc, n_seq * H));
+  size_t bytes = carry_bytes(n_seq, H) + (size_t)chunks * H * REC_BYTES;
+  // shapes that may take the segment scan (which keeps every record): room
+  // for its largest form
+  if (nc >= kScanMinChunks && (long long)n_seq * H <= kScanMaxChains)
     bytes = std::max(bytes, scan_workspace_bytes(n_seq, T_or_total, H, kScanMaxSegs));
   return bytes;
 }
