@@ -115,9 +115,14 @@ KDA_API kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v,
                            cudaStream_t stream);
 
 /* Bytes of device workspace kda_chunk_fwd needs for this shape:
- * B * ceil(T / 64) * H * 66560 + B * H * 65536 + 256, or, for shapes that
- * may take the segment scan (ceil(T / 64) >= 2048 and B * H <= 64), that of
- * kda_chunk_fwd_segments with 8 segments when it is larger. */
+ * R * H * 66560 + B * H * 65536 + 256 with R = B * ceil(T / 64) records per
+ * head, or, for shapes that may take the segment scan (ceil(T / 64) >= 2048
+ * and B * H <= 64), that of kda_chunk_fwd_segments with 8 segments when it
+ * is larger.  Where one record per chunk would pass 4 GiB and the call runs
+ * as overlapped segments (ceil(T / 64) >= 128 and B * H at most half the
+ * SMs), the records live in a ring of two segments of at most 128 chunks
+ * (R = B * 2 * segment, the ring under 1 GiB), so the size stops growing
+ * with T.  The answer depends on the current device's SM count. */
 KDA_API size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /*
