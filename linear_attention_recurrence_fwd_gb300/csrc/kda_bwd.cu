@@ -14,7 +14,7 @@
 //   G    = Diag(alpha_t) dS'                  (gradient of S_{t-1}).
 //
 // Layout of the work: the forward (the chunked tensor-core path) saves the
-// state at every chunk boundary; one CTA per (sequence, head, block of 16
+// state at every chunk boundary; one CTA per (sequence, head, block of 8
 // value columns) then walks the chunks from last to first.  For each chunk
 // it recomputes the 64 token states in fp32 from the saved chunk-start state
 // (S'_t to a per-CTA scratch in global memory, u_t and w_t to shared
@@ -54,7 +54,7 @@ struct BwdParams {
 // only the gradients summed along a row (dq, dk, dlog_alpha, dbeta) combine
 // the blocks, by atomic adds into zeroed buffers.  Thread c owns key row c
 // and the block's CB columns.
-constexpr int CB = 16;
+constexpr int CB = 8;
 
 template <int DIN>
 struct BwdShape {
@@ -80,15 +80,17 @@ __device__ __forceinline__ float bfv(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
 }
 
-// Sum of x over the warp's 32 rows for each of the CB = 16 columns: a
-// reduce-scatter over lane bits 4..1 leaves lanes 2 l and 2 l + 1 with
-// partial sums of column l, which one more exchange adds; lane 2 l writes
-// red[warp][l].  The caller synchronises and adds the warps.
-static_assert(CB == 16, "column_partials is written for 16 columns");
+// Sum of x over the warp's 32 rows for each of the CB columns: a
+// reduce-scatter over lane bits 4, 3, .. (one halving per bit, log2 CB
+// steps) leaves the lanes that differ only in the remaining low bits with
+// partial sums of one column, which a few exchanges add; the first of them
+// writes red[warp][column].  The caller synchronises and adds the warps.
+static_assert(CB == 8 || CB == 16 || CB == 32, "column blocks of 8, 16 or 32");
+constexpr int LOG_CB = CB == 8 ? 3 : CB == 16 ? 4 : 5;
 __device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int warp, int lane) {
 #pragma unroll
-  for (int step = 0; step < 4; ++step) {
-    const int bit = 16 >> step;         // lane bit 4, 3, 2, 1
+  for (int step = 0; step < LOG_CB; ++step) {
+    const int bit = 16 >> step;         // lane bit 4, 3, ...
     const int half = CB >> (step + 1);  // values kept after this step
     const bool up = (lane & bit) != 0;  // keep the upper half of the current range
 #pragma unroll
@@ -99,8 +101,10 @@ __device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int 
       x[i] = keep;
     }
   }
-  x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
-  if ((lane & 1) == 0) red[warp * CB + (lane >> 1)] = x[0];  // column 8 b4 + 4 b3 + 2 b2 + b1
+  constexpr int LOW = 5 - LOG_CB;  // lane bits left: the same column on 2^LOW lanes
+#pragma unroll
+  for (int o = 1; o < (1 << LOW); o <<= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
+  if ((lane & ((1 << LOW) - 1)) == 0) red[warp * CB + (lane >> LOW)] = x[0];
 }
 
 template <int DIN>
