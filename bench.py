@@ -352,8 +352,8 @@ def run_profile_case(local):
     """Small, fixed case for ncu captures (a few GB on the device at most):
     two prefills of B=1 T=32768 H=32 (long enough for the overlapped,
     segmented schedule), two of the 8k workload (plain two-stage schedule),
-    three decode steps, then one prefill of B=1 T=131072 H=4, which takes
-    the segment scan."""
+    three decode steps, one prefill of B=1 T=131072 H=4, which takes the
+    segment scan, then one backward of B=1 T=2048 H=32."""
     from linear_attention_recurrence_fwd_gb300 import binding
     from linear_attention_recurrence_fwd_gb300 import inputs as gen
 
@@ -379,6 +379,13 @@ def run_profile_case(local):
     del xd, d, o
     x = gen.make_inputs(1, 1 << 17, 4, 128, 128, 3, decay_mean=2.0, device=dev)
     binding.kda_chunk_fwd(*[x[k] for k in ("q", "k", "v", "log_alpha", "beta")], None)
+    torch.cuda.synchronize()
+    del x
+    x = gen.make_inputs(1, 2048, 32, 128, 128, 4, init_std=0.02, device=dev)
+    d_out = torch.randn((1, 2048, 32, 128), dtype=torch.float32, device=dev,
+                        generator=torch.Generator(device=dev).manual_seed(4))
+    binding.kda_chunk_bwd(*[x[k] for k in ("q", "k", "v", "log_alpha", "beta")], d_out,
+                          initial_state=x["initial_state"])
     torch.cuda.synchronize()
     if binding.kda_last_device_status() != 0:
         raise SystemExit("device status error")
