@@ -5,7 +5,8 @@ Every gradient (q, k, v, log_alpha, beta and the initial state) is compared
 element by element with the bar of tests/parity.py, each against its own
 RMS: several chunks and a ragged tail, a single partial chunk, d = 64 with
 two sequences, no initial state and no final-state gradient, slow decay (the
-gradient carries across every chunk), scale != 1, and the empty sequence.
+gradient carries across every chunk), scale != 1, the empty sequence, and
+the 8k x 32-head problem the bench times (three heads against the oracle).
 """
 import numpy as np
 import pytest
@@ -105,3 +106,28 @@ def test_backward_equals_autograd_of_the_forward_on_a_tiny_case():
     for name in GRADS:
         assert_output_close(got[name], leaf[name].grad, what=f"d{name} vs autograd")
     assert_state_close(got["initial_state"], s0.grad, what="d initial_state vs autograd")
+
+
+def test_backward_of_the_8k_bench_problem_on_sampled_heads():
+    """The configuration the bench times (B=1, T=8192, H=32, the prefill_8k
+    inputs and seed, random d_out): every head is computed on the GPU; three
+    heads (first, a middle one, last) are compared with the oracle in full
+    (heads are independent, so the oracle takes only those)."""
+    w = gen.WORKLOADS["prefill_8k"]
+    x = gen.workload_inputs(w)
+    r = np.random.default_rng(w.seed + 2)
+    d_out = torch.from_numpy(r.standard_normal((w.B, w.T, w.H, w.dv)).astype(np.float32))
+    g = {k: x[k].cuda() for k in KEYS}
+    got = binding.kda_chunk_bwd(*[g[k] for k in KEYS], d_out.cuda(),
+                                initial_state=x["initial_state"].cuda())
+    torch.cuda.synchronize()
+    assert binding.kda_last_device_status() == 0
+    got = {k: (v.cpu() if v is not None else None) for k, v in got.items()}
+    for h in (0, 17, 31):
+        hs = slice(h, h + 1)
+        ref = orc.kda_recurrence_bwd(*[x[k][:, :, hs] for k in KEYS], x["initial_state"][:, hs],
+                                     d_out[:, :, hs])
+        for name in GRADS:
+            assert_output_close(got[name][:, :, hs], ref[name], what=f"d{name} head {h}")
+        assert_state_close(got["initial_state"][:, hs], ref["initial_state"],
+                           what=f"d initial_state head {h}")
