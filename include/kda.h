@@ -186,6 +186,34 @@ KDA_API kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, co
                                                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_chunk_fwd_host -- kda_chunk_fwd with the tensors in host memory: the
+ * inputs q, k, v, log_alpha, beta and initial_state, and the outputs out and
+ * final_state, are host pointers (page-locked memory for the copies to run
+ * asynchronously; pageable memory works, with copies that block the calling
+ * thread).  Shapes, dtypes, results and errors are those of kda_chunk_fwd,
+ * without the segment scan (long sequences with few heads run as one serial
+ * pass per sequence and head).
+ *   workspace : device memory of kda_chunk_fwd_host_workspace_size() bytes,
+ *               16-byte aligned, owned by the caller: device copies of every
+ *               input and output, then kda_chunk_fwd's workspace.
+ * The prefill runs in rounds of chunks (its segments); the copies follow
+ * them: each round's token rows are copied in on a copy stream while earlier
+ * rounds compute, and its output rows are copied back on another copy stream
+ * once the round's state pass ends.  The call is asynchronous on `stream`:
+ * work queued on `stream` afterwards starts only when every copy back has
+ * landed.  The two copy streams are made once per device and kept for the
+ * life of the process.
+ */
+KDA_API kda_status_t kda_chunk_fwd_host(const void* q, const void* k, const void* v,
+                                        const void* log_alpha, const void* beta,
+                                        const float* initial_state, void* out,
+                                        kda_dtype_t out_dtype, float* final_state, int B, int T,
+                                        int H, int d_k, int d_v, float scale, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+KDA_API size_t kda_chunk_fwd_host_workspace_size(int B, int T, int H, int d_k, int d_v,
+                                                 kda_dtype_t out_dtype);
+
+/*
  * kda_chunk_bwd -- backward of kda_chunk_fwd, for training: the gradients of
  *   L = <d_out, out> + <d_final_state, final_state>
  * with respect to q, k, v, log_alpha, beta and initial_state.  The pages give

@@ -28,6 +28,7 @@ EXPORTS = ["kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_noall
            "kda_chunk_fwd_segments", "kda_chunk_fwd_segments_workspace_size",
            "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_launches", "kda_decode_verify",
            "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
+           "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size",
            "kda_decode_commit",
            "kda_varlen_fwd",
            "kda_varlen_fwd_workspace_size", "kda_decode_step", "kda_status_string",
@@ -60,6 +61,10 @@ def load(path: str = LIB_PATH):
         lib.kda_chunk_fwd_checkpointed.argtypes = ([_vp] * 7 + [_i, _vp, _i, _i, _i, _i, _i, _f] +
                                                    [_vp, _i, _vp, _sz, _vp])
         lib.kda_chunk_fwd_checkpointed.restype = _i
+        lib.kda_chunk_fwd_host.argtypes = lib.kda_chunk_fwd.argtypes
+        lib.kda_chunk_fwd_host.restype = _i
+        lib.kda_chunk_fwd_host_workspace_size.argtypes = [_i] * 6
+        lib.kda_chunk_fwd_host_workspace_size.restype = _sz
         lib.kda_chunk_bwd.argtypes = [_vp] * 14 + [_i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
         lib.kda_chunk_bwd.restype = _i
         lib.kda_chunk_bwd_workspace_size.argtypes = [_i] * 5
@@ -141,6 +146,11 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _need_host(t, dtype, name):
+    if t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host {dtype} tensor")
+
+
 def kda_chunk_fwd(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
                   out_dtype=torch.float32, output_final_state=True, out=None,
                   final_state=None, stream=None):
@@ -219,6 +229,40 @@ def kda_chunk_fwd_checkpointed(q, k, v, log_alpha, beta, initial_state=None, sca
         _p(checkpoints) if n_ckpt else None, int(checkpoint_every), _p(ws), ws_bytes,
         _stream(stream)), "kda_chunk_fwd_checkpointed")
     return out, final_state, checkpoints
+
+
+def kda_chunk_fwd_host_workspace(B, T, H, dk=128, dv=128, out_dtype=torch.float32, device=None):
+    """A device workspace for kda_chunk_fwd_host of this shape."""
+    lib = load()
+    n = lib.kda_chunk_fwd_host_workspace_size(B, T, H, dk, dv, _dtype_code(out_dtype))
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, initial_state=None, scale=1.0,
+                       out_dtype=torch.float32, out=None, final_state=None, workspace=None,
+                       stream=None):
+    """kda_chunk_fwd with every tensor in host memory (CPU tensors, ideally
+    pinned): the library copies each round's inputs in and its outputs back
+    while other rounds compute.  Returns (out, final_state) on the host."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_alpha, "log_alpha"), (beta, "beta")):
+        _need_host(t, torch.bfloat16, n)
+    if initial_state is not None:
+        _need_host(initial_state, torch.float32, "initial_state")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, pin_memory=pin)
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, pin_memory=pin)
+    if workspace is None:
+        workspace = kda_chunk_fwd_host_workspace(B, T, H, dk, dv, out.dtype)
+    _check(lib.kda_chunk_fwd_host(
+        _p(q), _p(k), _p(v), _p(log_alpha), _p(beta), _p(initial_state), _p(out),
+        _dtype_code(out.dtype), _p(final_state), B, T, H, dk, dv, float(scale), _p(workspace),
+        workspace.numel(), _stream(stream)), "kda_chunk_fwd_host")
+    return out, final_state
 
 
 def kda_chunk_bwd(q, k, v, log_alpha, beta, d_out, initial_state=None, d_final_state=None,

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libkda.so")
 PROBE_LIB = os.path.join(PKG, "libkda_probe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-PRODUCT_SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_chunk.cu", "kda_bwd.cu"]
+PRODUCT_SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_chunk.cu", "kda_bwd.cu", "kda_host.cu"]
 PROBE_SOURCES = ["kda_probe.cu"]
 
 

@@ -164,6 +164,34 @@ kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void
   return from_cuda(kda::launch_chunk_fwd(p, workspace, stream));
 }
 
+size_t kda_chunk_fwd_host_workspace_size(int B, int T, int H, int d_k, int d_v,
+                                         kda_dtype_t out_dtype) {
+  if (B <= 0 || T < 0 || H <= 0 || d_k != d_v || !(d_k == 128 || d_k == 64)) return 0;
+  if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return 0;
+  return kda::chunk_host_workspace_bytes(B, T, H, d_k, out_dtype == KDA_F32);
+}
+
+kda_status_t kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* log_alpha,
+                                const void* beta, const float* initial_state, void* out,
+                                kda_dtype_t out_dtype, float* final_state, int B, int T, int H,
+                                int d_k, int d_v, float scale, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+  const bool has_tokens = (long long)B * T > 0;
+  if (has_tokens && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (H <= 0 || d_k <= 0 || d_v <= 0) return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_BF16 && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (d_k != d_v || !(d_k == 128 || d_k == 64)) return KDA_ERR_UNSUPPORTED;
+  if ((long long)B * T > 0x7fffffffLL || work_items(B, T, H) > kMaxItems) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  const size_t need = kda_chunk_fwd_host_workspace_size(B, T, H, d_k, d_v, out_dtype);
+  if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+  kda::ChunkProblem p{q, k, v, log_alpha, beta, initial_state, out, out_dtype == KDA_F32,
+                      final_state, nullptr, B, T, B * T, H, d_k, scale, check_decay_env(), false};
+  return from_cuda(kda::launch_chunk_fwd_host(p, workspace, stream));
+}
+
 size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v) {
   if (B <= 0 || T <= 0 || H <= 0 || d_k != d_v || !(d_k == 128 || d_k == 64)) return 0;
   return kda::chunk_bwd_workspace_bytes(B, T, H, d_k);

@@ -1569,11 +1569,14 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
       : pr.n_seq * pr.H;
   const bool overlap = allow_overlap && carry && grid_done &&
                        use_overlap(segs > 1 ? long_chains / 2 : long_chains, nc_max, sms);
+  RoundHooks* hooks = segs == 1 && !pr.cu_seqlens ? pr.hooks : nullptr;
   if (!overlap) {
     const bool persistent = grid_done != nullptr;
     if (persistent) e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
+    if (e == cudaSuccess && hooks) e = hooks->before_round(0, nc_max, stream);
     if (e == cudaSuccess) e = intra(0, nc_max, false, persistent);
     if (e == cudaSuccess) e = state(0, nc_max, first_phase);
+    if (e == cudaSuccess && hooks) e = hooks->after_round(0, nc_max, stream);
     if (e == cudaSuccess) e = finish_scan();
     return e;
   }
@@ -1588,8 +1591,10 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   e = cudaMemsetAsync(grid_done, 0, 2 * sizeof(int), stream);
   for (int j_lo = 0; e == cudaSuccess && j_lo < nc_max; j_lo += seg) {
     const int len = std::min(seg, nc_max - j_lo);
-    e = intra(j_lo, len, j_lo > 0, true);
+    if (hooks) e = hooks->before_round(j_lo, len, stream);
+    if (e == cudaSuccess) e = intra(j_lo, len, j_lo > 0, true);
     if (e == cudaSuccess) e = state(j_lo, j_lo + len, first_phase);
+    if (e == cudaSuccess && hooks) e = hooks->after_round(j_lo, len, stream);
   }
   if (e == cudaSuccess) e = finish_scan();
   return e;

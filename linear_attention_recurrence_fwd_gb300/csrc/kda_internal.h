@@ -23,6 +23,17 @@ cudaError_t launch_decode_tokens(const void* q, const void* k, const void* v,
 // Chunked prefill over either B fixed-length sequences (cu_seqlens == null,
 // every sequence T tokens, tensors [B,T,H,d]) or N packed sequences
 // (cu_seqlens on the device, tensors [T_total,H,d]).
+// Called by the prefill's schedule around each of its rounds (chunks
+// [j_lo, j_lo + len) of every sequence), on the compute stream: before the
+// round's intra-chunk stage is launched, and after its state pass is.
+struct RoundHooks {
+  virtual cudaError_t before_round(int j_lo, int len, cudaStream_t stream) = 0;
+  virtual cudaError_t after_round(int j_lo, int len, cudaStream_t stream) = 0;
+
+ protected:
+  ~RoundHooks() = default;
+};
+
 struct ChunkProblem {
   const void *q, *k, *v, *log_alpha, *beta;
   const float* initial_state;
@@ -44,6 +55,8 @@ struct ChunkProblem {
   // segment scan of fixed-length sequences: -1 lets the library choose, 0
   // or 1 asks for none, more asks for that many segments of whole chunks
   int scan_segs;
+  // per-round callbacks (fixed lengths without a scan only), or null
+  RoundHooks* hooks = nullptr;
 };
 
 // Device workspace the chunked prefill needs: per-(chunk, head) records
@@ -53,6 +66,14 @@ size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H
 size_t chunk_scan_workspace_bytes(int B, long long T, int H, int segs);
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
+
+// kda_chunk_fwd on host buffers: the inputs are copied in round by round on
+// a copy stream while earlier rounds compute, and each round's outputs are
+// copied back as soon as its state pass ends.  fwd holds host pointers; the
+// device workspace holds device copies of every input and output, then the
+// prefill's own workspace.
+size_t chunk_host_workspace_bytes(int B, int T, int H, int d, bool out_f32);
+cudaError_t launch_chunk_fwd_host(const ChunkProblem& fwd, void* workspace, cudaStream_t stream);
 
 // Backward of the fixed-length prefill described by fwd (its out and
 // final_state are ignored): the forward again for the state at every chunk
