@@ -174,10 +174,11 @@ __device__ __forceinline__ void st8h(uint32_t addr, const float* x) {
 }
 // x rounded to nearest tf32 (10 explicit mantissa bits), as the bit pattern
 // of an fp32 whose low 13 bits are zero.
+// Adding half of the dropped unit to the bit pattern rounds the magnitude to
+// nearest with ties away from zero (a carry into the exponent is the correct
+// rounding up); the mask clears the 13 bits the product ignores.
 __device__ __forceinline__ float tf32r(float x) {
-  uint32_t y;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-  return __uint_as_float(y);
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 __device__ __forceinline__ void st_f32(uint32_t addr, float x) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
@@ -523,13 +524,16 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     return it;
   };
   int* s_item = reinterpret_cast<int*>(sbp + A_MISC + 24);
-  // next item: from the shared counter, else a fixed stride over the grid.
-  // The first barrier keeps the write behind every read of the previous
-  // value (an empty item skips the body's barriers).
-  auto next_item = [&](int w) -> int {
+  // next item: from the shared counter (thread 0 takes a ticket with claim()
+  // some time before next_item needs it, so the atomic's round trip overlaps
+  // work), else a fixed stride over the grid.  The first barrier keeps the
+  // write behind every read of the previous value (an empty item skips the
+  // body's barriers).
+  auto claim = [&]() -> int { return tid == 0 && p.grid_done ? atomicAdd(p.grid_done + 1, 1) : 0; };
+  auto next_item = [&](int w, int ticket) -> int {
     if (!p.grid_done) return w + gridDim.x;
     __syncthreads();
-    if (tid == 0) *s_item = atomicAdd(p.grid_done + 1, 1);
+    if (tid == 0) *s_item = ticket;
     __syncthreads();
     return *s_item;
   };
@@ -555,13 +559,13 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     }
     return true;
   };
-  int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x);
+  int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x, claim());
   float beta_t;
   bool pending = prefetch(w, beta_t);
   while (ok && w < p.n_items) {
   const Item cur = item_of(w);
   if (cur.valid <= 0) {
-    w = next_item(w);
+    w = next_item(w, claim());
     pending = prefetch(w, beta_t);
     continue;
   }
@@ -783,6 +787,8 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
       bulk_commit();
     }
+    // the ticket for the item after this one, read once the solve is done
+    const int ticket = claim();
 
     // ---- T = (I + A_kk)^-1, unit lower triangular, in fp32.  L = I + A_kk is
     // read transposed (akk[i][r] = L[r][i]); T lives in ti with its 16-byte
@@ -811,7 +817,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     solve_offdiag(akk, ti, dinv, tid);
     // the next item's inputs land where this item's first record stores read
     // (and in A_RG1): once those reads are done, issue them
-    w_next = next_item(w);
+    w_next = next_item(w, ticket);
     if (tid == 0) bulk_wait_reads();
     pending_next = prefetch(w_next, beta_next);
     // ---- T diag(beta) in bf16 (rows r, K = i), lower triangle only
