@@ -1070,7 +1070,6 @@ __global__ void __launch_bounds__(B_THREADS, 1)
     // ---------------- issuer: one lane issues every MMA and every load
     if ((tid & 31) == 0 && nchunks > 0) {
       constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
-      constexpr uint32_t ID_D = make_idesc(128, 128, false, true, true, true);    // fp16, -A
       constexpr uint32_t ID_O2 = make_idesc(128, 64, false, true, true, true);    // fp16, -A
       constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
       // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is
@@ -1100,17 +1099,20 @@ __global__ void __launch_bounds__(B_THREADS, 1)
         if (!(ok = mbar_wait(st_ready, j & 1))) break;
         if (j >= 2 && !(ok = mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1))) break;
         tc_fence_after_sync();
-        {  // M4 and the first half of M5 as one N = 128 product: W and q e^g are
-           // adjacent MN-major operands (the second 64-row block of N sits one
-           // leading-byte offset, 16 KB, after the first), so
-           //   D = -S^T [W; q e^g]^T = [-S^T W^T | -S^T (q e^g)^T]
-           // reads the S^T operand from shared memory once for both.
+        {  // M4, D = -S^T W^T, alone (N = 64): the chain waits only for it.  The
+           // first half of M5, -S^T (q e^g)^T, follows into the next 64 columns
+           // and runs while the chain forms U^T.
           const uint64_t dst = layout_desc(ST, 0, 0);
-          const uint64_t dwq = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
+          const uint64_t dw = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
+          const uint64_t dq = layout_desc(mnmajor(rb + REC_QT, 16384), 0, 0);
 #pragma unroll
           for (int k0 = 0; k0 < DP; k0 += 16)
-            umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dwq, k0, true), ID_D, k0 > 0);
+            umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dw, k0, true), ID_O2, k0 > 0);
           umma_commit(mma_a);
+#pragma unroll
+          for (int k0 = 0; k0 < DP; k0 += 16)
+            umma_bf16(td + 64, desc_adv(dst, k0, false, 16384), desc_adv(dq, k0, true), ID_O2,
+                      k0 > 0);
         }
         if (!(ok = mbar_wait(ut_ready, j & 1))) break;
         tc_fence_after_sync();
