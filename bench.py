@@ -564,7 +564,10 @@ def main():
         "e2e": {"value": e2e_value, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_call,
-        "gpu_launches_note": f"{launches_per_call} per prefill call (intra-chunk stage and state "
+        "gpu_launches_note": f"{launches_per_call} per prefill call (the fused launch: state "
+                             f"chains and intra-chunk stage in one cooperative grid)"
+                             if launches_per_call == 1 else
+                             f"{launches_per_call} per prefill call (intra-chunk stage and state "
                              f"pass, per round of the overlapped schedule)",
         "workloads": extra,
         "clocks": clocks,

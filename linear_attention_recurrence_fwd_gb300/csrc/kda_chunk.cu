@@ -61,6 +61,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
+#include <cstdlib>
 #include <mutex>
 
 #include "kda_internal.h"
@@ -281,9 +283,10 @@ __device__ __forceinline__ int tix(int r, int c) {
 // Four phases: P = L_{b+1,b} T_bb and T_{b+1,b} = -T_{b+1,b+1} P for b = 0
 // and 2 (P in the unused block (b, b+1) of ti), then X = L_C T1 (block
 // (kb, cb) of X in the unused block (cb, kb)), then -T2 X.  A thread owns a
-// strip of 4 columns of one row; each phase ends in a CTA barrier.
+// strip of 4 columns of one row; each phase ends in the body's barrier (sync).
+template <class Sync>
 __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const float* dinv,
-                                              int tid) {
+                                              int tid, Sync&& sync) {
   if (tid < 128) {
     const int b = 2 * (tid >> 6), a = b + 1, rr = (tid >> 2) & 15, q = tid & 3;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -298,7 +301,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     }
     *reinterpret_cast<float4*>(ti + tix(16 * b + rr, 16 * a + 4 * q)) = acc;
   }
-  __syncthreads();
+  sync();
   if (tid < 128) {
     const int b = 2 * (tid >> 6), a = b + 1, rr = (tid >> 2) & 15, q = tid & 3;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -314,7 +317,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     *reinterpret_cast<float4*>(ti + tix(16 * a + rr, 16 * b + 4 * q)) =
         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
-  __syncthreads();
+  sync();
   {  // X = L_C T1: rows r in [32, 64), columns of block cb; T1 is zero above its diagonal blocks
     const int cb = tid >> 7, r = 32 + ((tid >> 2) & 31), c0 = 16 * cb + 4 * (tid & 3);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -334,7 +337,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     for (int m = 16; m < 32; ++m) term(m);
     *reinterpret_cast<float4*>(ti + tix(16 * cb + (r & 15), 16 * (r >> 4) + (c0 & 15))) = acc;
   }
-  __syncthreads();
+  sync();
   {  // -T2 X: rows r of block 2 + rb, columns of block cb; T2 is zero above its diagonal blocks
     const int rb = tid >> 7, cb = (tid >> 6) & 1;
     const int r = 32 + 16 * rb + ((tid >> 2) & 15), c0 = 16 * cb + 4 * (tid & 3);
@@ -355,7 +358,7 @@ __device__ __forceinline__ void solve_offdiag(const float* akk, float* ti, const
     }
     *reinterpret_cast<float4*>(ti + tix(r, c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
-  __syncthreads();
+  sync();
 }
 
 // Position pair pidx of the ablation: tile a, row rr and column ii <= rr.
@@ -378,9 +381,10 @@ __device__ __forceinline__ void pair_of(int pidx, int& a, int& rr, int& ii) {
 // one thread per position pair walks the channels starting at a
 // thread-dependent offset so a warp's loads fall in distinct banks.  Pair
 // pidx = tid + 256 n (of 4 x 136) leaves A_qk in aq[n] and A_kk in ak[n].
-// Called by all threads of the CTA.
+// Called by all 256 threads of a stage-1 body; sync is its barrier.
+template <class Sync>
 __device__ __forceinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t tl, int tid,
-                                                        float (&aq)[3], float (&ak)[3]) {
+                                                        float (&aq)[3], float (&ak)[3], Sync&& sync) {
   uint16_t* sq = reinterpret_cast<uint16_t*>(sbp);
   uint16_t* sk = reinterpret_cast<uint16_t*>(sbp + 16384);
   float* sg = reinterpret_cast<float*>(sbp + 32768);
@@ -399,7 +403,7 @@ __device__ __forceinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t t
       sg[(t0 + j) * DP + c] = gv[j];
     }
   }
-  __syncthreads();
+  sync();
 #pragma unroll
   for (int n = 0; n < 3; ++n) {
     const int pidx = tid + A_THREADS * n;
@@ -420,7 +424,70 @@ __device__ __forceinline__ void diagonal_tiles_per_pair(uint8_t* sbp, uint32_t t
     aq[n] = aqs;
     ak[n] = aks;
   }
-  __syncthreads();
+  sync();
+}
+
+// The fused single-launch prefill (kda_fused_kernel): one CTA per SM, the
+// first B * H CTAs walk the state chains and the others run two stage-1
+// items at a time, in chunk order, into a ring of R records per chain.
+//   ready[c][s]  = j + 1 once the record of chunk j of chain c is complete in
+//                  slot s = j % R (stage 1 publishes, the chain waits);
+//   consumed[c]  = the chunks of chain c whose records have been copied into
+//                  the chain's shared memory (the chain publishes; stage 1
+//                  waits before it overwrites a slot);
+//   counter      = the next stage-1 item (chunk-major: item w is chunk
+//                  w / (B H) of chain w % (B H)).
+// All three start at zero.  Each of them, and each chain's ready slots, has
+// a 128-byte line of its own (kFlagLine ints apart), so that polls of one
+// flag do not slow the stores and polls of the others.  The grid is a
+// cooperative launch, so every CTA is resident and a wait on another role
+// always ends; each wait is bounded all the same.
+constexpr int kFlagLine = 32;  // ints per 128-byte line
+struct FusedRing {
+  int* ready;     // chain c's slots at ready + c * ready_stride
+  int* consumed;  // chain c's at consumed + c * kFlagLine
+  int* counter;
+  int R, ready_stride;
+};
+
+// Orders this thread's global accesses between the generic proxy (the flags)
+// and the async proxy (bulk copies of the records).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_relaxed_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int* ptr, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+// Waits until *ptr >= want, for at most two seconds of wall time; `seen` is a
+// value of *ptr read earlier (a load issued ahead of need).  Relaxed loads:
+// a GPU-scope load reads the coherent copy in L2, and what depends on the
+// flag is a bulk copy, issued only once the value has been seen, that reads
+// L2 too, where the producer's completed stores were before it published.
+// A waiter that can afford latency backs off (sleeps doubling from 256 ns
+// to 4 us), which keeps many waiters from crowding the flag's line.
+__device__ __forceinline__ bool poll_at_least(const int* ptr, int want, int seen,
+                                              bool backoff = false) {
+  if (seen >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t ns = backoff ? 256 : 64;
+  while (true) {
+    if (ld_relaxed_gpu(ptr) >= want) return true;
+    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    __nanosleep(ns);
+    if (backoff && ns < 4096) ns *= 2;
+  }
+}
+// Named barrier `id` over `n` threads (a part of the CTA).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // Stage 1 work list: item w = ((n * seg_len) + (j - j_lo)) * H + h covers
@@ -443,14 +510,23 @@ struct IntraParams {
 
 // RING: records in a ring (p.rec_stride, p.rec_shift); a separate
 // instantiation, so that the others carry none of it.
-template <int DIN, bool PAIRS, bool RING = false>
-__global__ void __launch_bounds__(A_THREADS, 2)
-    kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
-  // Two CTAs per SM loop over (chunk, head) items: taken from a counter
-  // (a persistent grid), or without one at a fixed stride over the grid.
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const int tid = threadIdx.x, warp = tid >> 5;
+// The intra-chunk stage run by 256 threads (tid 0..255) over smem_raw: a
+// whole CTA of kda_intra_kernel, or one half of a fused CTA (FUSED), whose
+// barrier is then the named barrier bar_id over those 256 threads.
+template <int DIN, bool PAIRS, bool RING, bool FUSED, typename Params>
+__device__ __forceinline__ void intra_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                           const CUtensorMap& tm_g, Params p, const FusedRing& ring,
+                                           uint8_t* smem_raw, const int tid, const uint32_t bar_id) {
+  // Two CTAs (or CTA halves) per SM loop over (chunk, head) items: taken
+  // from a counter (a persistent grid), or without one at a fixed stride
+  // over the grid.
+  const int warp = tid >> 5;
+  auto csync = [&]() {
+    if (FUSED)
+      named_sync(bar_id, A_THREADS);
+    else
+      __syncthreads();
+  };
   const int c = tid & (DP - 1), hh = tid >> 7;  // key channel (TMEM lane); token half
   const int ta[2] = {hh ? 1 : 0, hh ? 2 : 3};   // the token tiles this thread owns
   const int H = p.H;
@@ -461,6 +537,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + A_MISC + 16);
   int* s_abort = reinterpret_cast<int*>(sbp + A_MISC + 20);
+  int* s_pub = reinterpret_cast<int*>(sbp + A_MISC + 32);  // fused: {chain, chunk} to publish
   float* s_beta = reinterpret_cast<float*>(sbp + A_MISC + 64);    // [64]
   float* s_gamma = reinterpret_cast<float*>(sbp + A_MISC + 512);  // [128], 16-byte aligned
 
@@ -469,13 +546,14 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     mbar_init(bar_mma, 1);
     mbar_fence_init();
     *s_abort = 0;
+    s_pub[1] = -1;
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_s, TA_COLS);
-    tmem_relinquish();
+    if (!FUSED) tmem_relinquish();  // (a fused CTA has a second allocation to make)
   }
   tc_fence_before_sync();
-  __syncthreads();
+  csync();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_s;
   const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -488,29 +566,39 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       set_status(6);
     }
     phase ^= 1u;
-    __syncthreads();
+    csync();
     tc_fence_after_sync();
     return *s_abort == 0;
   };
   auto operands_ready = [&]() {
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
+    csync();
     tc_fence_after_sync();
   };
 
   // item w -> head, first token, valid tokens and record index (valid <= 0:
   // past the end of a packed sequence)
   struct Item {
-    int h, t0, valid, qrec;
+    int h, t0, valid, qrec, chain, chunk;
   };
   auto item_of = [&](int w) {
-    Item it;
+    Item it{};
     it.h = w % H;
     const int item_r = w / H;
-    const int n = item_r / p.seg_len, jc = p.j_lo + item_r % p.seg_len;
+    int n = item_r / p.seg_len, jc = p.j_lo + item_r % p.seg_len;
+    if (FUSED) {  // chunk-major: all chains of chunk j before chunk j + 1
+      it.chain = w % (p.n_seq * H);
+      n = it.chain / H;
+      jc = w / (p.n_seq * H);
+    }
+    it.chunk = jc;
     int seq0, len;
-    if (p.plan) {
+    if (FUSED) {
+      seq0 = n * p.T;
+      len = p.T;
+      it.qrec = n * ring.R + jc % ring.R;
+    } else if (p.plan) {
       seq0 = p.plan[p.n_seq + 1 + n];
       len = p.plan[2 * p.n_seq + 1 + n];
       it.qrec = p.plan[n] + jc;
@@ -529,12 +617,13 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   // work), else a fixed stride over the grid.  The first barrier keeps the
   // write behind every read of the previous value (an empty item skips the
   // body's barriers).
-  auto claim = [&]() -> int { return tid == 0 && p.grid_done ? atomicAdd(p.grid_done + 1, 1) : 0; };
+  int* const counter = FUSED ? ring.counter : p.grid_done ? p.grid_done + 1 : nullptr;
+  auto claim = [&]() -> int { return tid == 0 && counter ? atomicAdd(counter, 1) : 0; };
   auto next_item = [&](int w, int ticket) -> int {
-    if (!p.grid_done) return w + gridDim.x;
-    __syncthreads();
+    if (!counter) return w + gridDim.x;
+    csync();
     if (tid == 0) *s_item = ticket;
-    __syncthreads();
+    csync();
     return *s_item;
   };
   // The inputs of item w: thread 0 issues the TMA loads of its q, k and log
@@ -559,7 +648,22 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     }
     return true;
   };
-  int w = next_item(p.grid_done ? 0 : (int)blockIdx.x - (int)gridDim.x, claim());
+  int w = next_item(counter ? 0 : (int)blockIdx.x - (int)gridDim.x, claim());
+  // Fused: thread 0 publishes a record once its bulk stores have completed,
+  // some time after it issued them (the wait then costs nothing), and while
+  // the next item's first product runs (which hides part of the release).
+  // The bytes and the flag reach L2 by different paths, so the flag is a
+  // release at GPU scope: a chain that sees it finds the bytes there.  Every
+  // record is published before its body can wait for a ring slot, so no
+  // record waits behind another chain's progress.
+  auto publish = [&]() {  // thread 0
+    bulk_wait_all();
+    fence_proxy_async_global();
+    if (s_pub[1] >= 0) {
+      st_release_gpu(ring.ready + s_pub[0] * ring.ready_stride + s_pub[1] % ring.R, s_pub[1] + 1);
+      s_pub[1] = -1;
+    }
+  };
   float beta_t;
   bool pending = prefetch(w, beta_t);
   while (ok && w < p.n_items) {
@@ -570,6 +674,9 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     continue;
   }
   const int h = cur.h, valid = cur.valid, qrec = cur.qrec;
+  // fused: the chain's progress as of now, read ahead of the first store
+  const int consumed_seen =
+      FUSED && tid == 0 ? ld_relaxed_gpu(ring.consumed + cur.chain * kFlagLine) : 0;
   uint8_t* rec = p.records + ((size_t)qrec * H + h) * REC_BYTES;
   int w_next = p.n_items;
   float beta_next = 0.f;
@@ -602,7 +709,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   if (tid < CH) s_beta[tid] = beta_t;
   fence_proxy_async_smem();
   tc_fence_before_sync();
-  __syncthreads();
+  csync();
   tc_fence_after_sync();
 
   ok = wait_all(bar_tma, tma_phase);
@@ -656,10 +763,10 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   // the previous item's last stores read [56K, 64K) and [81K, 97K), which the
   // M1 operands (and the ablation's staging) below overwrite
   if (tid == 0) bulk_wait_reads();
-  __syncthreads();
+  csync();
   // ablation only: the diagonal tiles per position pair, while g is in TMEM
   float pq[3], pk[3];
-  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, pq, pk);
+  if (PAIRS && ok) diagonal_tiles_per_pair(sbp, tl, tid, pq, pk, csync);
 
   // ---- M1 in two passes of one kind::tf32 product each, K-major fp32
   // operands: A = key rows under the references of two row tiles
@@ -684,6 +791,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       for (int k0 = 0; k0 < DP; k0 += 8)
         umma_tf32(d, layout_desc(XA, 0, k0), layout_desc(KBA, 0, k0), ID_M1, k0 > 0);
       umma_commit(bar_mma);
+      if (FUSED && pass == 0) publish();  // the previous item's record
     }
     ok = wait_all(bar_mma, mma_phase);
   }
@@ -739,7 +847,7 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       for (int r0 = 0; r0 < 16 * (c >> 4); r0 += 8) st8h(layout_addr(AQ, r0, c), z);
     }
     if (PAIRS) {  // the ablation's diagonal tiles replace the dense ones
-      __syncthreads();
+      csync();
 #pragma unroll
       for (int n = 0; n < 3; ++n) {
         const int pidx = tid + A_THREADS * n;
@@ -782,10 +890,19 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     }
     if (hh == 0) s_gamma[c] = ex2(E[3] * LOG2E);
     fence_proxy_async_smem();
-    __syncthreads();
+    csync();
     if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
-      bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
-      bulk_commit();
+      // fused: the slot's previous record (chunk - R) must have been copied in
+      const bool slot_free = !FUSED || poll_at_least(ring.consumed + cur.chain * kFlagLine,
+                                                     cur.chunk - ring.R + 1, consumed_seen, true);
+      if (slot_free) {
+        if (FUSED) fence_proxy_async_global();
+        bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
+        bulk_commit();
+      } else {
+        *s_abort = 1;
+        set_status(6);
+      }
     }
     // the ticket for the item after this one, read once the solve is done
     const int ticket = claim();
@@ -812,9 +929,9 @@ __global__ void __launch_bounds__(A_THREADS, 2)
 #pragma unroll
       for (int q = 0; q < 4; ++q) drow[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
-    __syncthreads();
+    csync();
     // off-diagonal blocks: T_10 and T_32, then the lower-left 32 x 32 block
-    solve_offdiag(akk, ti, dinv, tid);
+    solve_offdiag(akk, ti, dinv, tid, csync);
     // the next item's inputs land where this item's first record stores read
     // (and in A_RG1): once those reads are done, issue them
     w_next = next_item(w, ticket);
@@ -859,12 +976,16 @@ __global__ void __launch_bounds__(A_THREADS, 2)
     st8h(layout_addr(WT, 32 * hh + 16, c), w1);
     st8h(layout_addr(WT, 32 * hh + 24, c), w1 + 8);
     fence_proxy_async_smem();
-    __syncthreads();
+    csync();
     if (tid == 0) {
       bulk_s2g(rec + REC_WT, sb + A_WST, REC_QT - REC_WT);
       bulk_s2g(rec + REC_TB, sb + A_STG + REC_TB, REC_G - REC_TB);
       bulk_s2g(rec + REC_G, smem_u32(s_gamma), 512);
       bulk_commit();
+      if (FUSED) {
+        s_pub[0] = cur.chain;
+        s_pub[1] = cur.chunk;
+      }
     }
   }
   w = w_next;
@@ -873,11 +994,16 @@ __global__ void __launch_bounds__(A_THREADS, 2)
   }  // items
   // loads still in flight after a failed wait land before the CTA's memory goes away
   if (pending && tid == 0) mbar_wait(bar_tma, tma_phase);
-  if (tid == 0) bulk_wait_all();
+  if (tid == 0) {
+    if (FUSED)
+      publish();  // the last record
+    else
+      bulk_wait_all();
+  }
   tc_fence_before_sync();
-  __syncthreads();
+  csync();
   if (warp == 0) tmem_dealloc(tmem, TA_COLS);
-  if (p.grid_done && threadIdx.x == 0) {
+  if (!FUSED && p.grid_done && tid == 0) {
     // This grid was allowed to start before the previous segment's state
     // pass finished.  The CTA that finishes last waits for that grid, so
     // this grid completes only after it: the next state pass, which reads
@@ -889,6 +1015,15 @@ __global__ void __launch_bounds__(A_THREADS, 2)
       p.grid_done[1] = 0;
     }
   }
+}
+
+template <int DIN, bool PAIRS, bool RING = false>
+__global__ void __launch_bounds__(A_THREADS, 2)
+    kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_g, IntraParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  intra_body<DIN, PAIRS, RING, false, const IntraParams>(tm_q, tm_k, tm_g, p, FusedRing{}, smem_raw,
+                                                        threadIdx.x, 0);
 }
 
 // Stage 2 covers chunks [j_lo, j_hi) of every sequence.  The state entering
@@ -939,6 +1074,12 @@ constexpr int B_THREADS = B_CHAIN + B_OUTPUT + 32;
 // SCAN: the walks of a segment scan (p.phase 1 or 2); RING: records in a
 // ring (p.rec_stride, p.rec_shift).  The plain pass is a separate
 // instantiation so that it carries none of that logic.
+// A CTA of the fused launch (see FusedRing) runs either one state chain (its
+// first B_THREADS threads) or two stage-1 bodies.
+constexpr int F_THREADS = 2 * A_THREADS;
+constexpr uint32_t F_SMEM = 2 * A_SMEM > B_SMEM ? 2 * A_SMEM : B_SMEM;
+static_assert(F_THREADS >= B_THREADS, "the state pass fits a fused CTA");
+
 template <int DIN, typename OutT, bool SCAN, bool RING = false>
 __global__ void __launch_bounds__(B_THREADS, 1)
     kda_state_kernel(const __grid_constant__ CUtensorMap tm_v, StateParams p) {
@@ -1288,6 +1429,424 @@ __global__ void __launch_bounds__(B_THREADS, 1)
   if (warp == 0) tmem_dealloc(tmem, TB_COLS);
 }
 
+// The state pass of chain (sequence n, head h) in the fused launch, run by
+// the first B_THREADS threads of its CTA (barrier: named barrier 1): the
+// algorithm of kda_state_kernel above, with the records taken from the ring
+// once stage 1 has published them.  (The plain kernel keeps its own copy of
+// the code: compiled as one kernel function reading its own parameters, its
+// chain loop measured faster than in any shared form.)
+template <int DIN, typename OutT>
+__device__ __forceinline__ void fused_state_body(const CUtensorMap& tm_v, const StateParams& p,
+                                                 const FusedRing& ring, uint8_t* smem_raw,
+                                                 const int tid, const int n, const int h) {
+  constexpr bool SCAN = false, RING = false, FUSED = true;
+  const int warp = tid >> 5;
+  const int half = (warp >> 2) & 1;           // chain warps: which half of the columns
+  const int v = 32 * (warp & 3) + (tid & 31);  // TMEM lane = value channel
+  const int H = p.H;
+  auto csync = [&]() {
+    if (FUSED)
+      named_sync(1, B_THREADS);
+    else
+      __syncthreads();
+  };
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sbp = smem_raw + (sb - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbp + B_MISC);  // [2] record + v tile landed
+  uint64_t* mma_a = full + 2;     // D = -S^T [W; q e^g]^T done
+  uint64_t* mma_b = full + 3;     // S update and the rest of O done
+  uint64_t* o_full = full + 4;    // [2] output tile ready
+  uint64_t* o_empty = full + 6;   // [2] output tile drained
+  uint64_t* st_ready = full + 8;  // chain -> issuer: S^T operand written
+  uint64_t* ut_ready = full + 9;  // chain -> issuer: U^T operand written, state decayed
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sbp + B_MISC + 96);
+  int* s_abort = reinterpret_cast<int*>(sbp + B_MISC + 100);
+  int* s_range = reinterpret_cast<int*>(sbp + B_MISC + 104);
+
+  int tok0, len, base;
+  if (p.plan) {
+    tok0 = p.plan[p.n_seq + 1 + n];
+    len = p.plan[2 * p.n_seq + 1 + n];
+    base = p.plan[n];
+  } else {
+    tok0 = n * p.T;
+    len = p.T;
+    base = FUSED  ? n * ring.R
+           : RING ? n * p.rec_stride + p.rec_shift
+                  : n * ((p.T + CH - 1) / CH);
+  }
+  const int nch_seq = len > 0 ? (len + CH - 1) / CH : 0;
+  const int jb = p.j_lo, nchunks = max(0, min(p.j_hi, nch_seq) - jb);  // j below is jb + local
+  const size_t sbase = (size_t)(n * H + h) * DIN * DIN;
+  // the walk this CTA does: kind 0 the plain recurrence with outputs, 1 the
+  // transition (identity start, no values, no outputs), 2 the zero-start
+  // state (no outputs); and where its first state comes from and its last
+  // state goes
+  const int seg = SCAN ? n % p.segs : 0;
+  const size_t real = (size_t)((SCAN ? n / p.segs : n) * H + h) * DIN * DIN;
+  float* carry = p.carry ? p.carry + 0 + sbase : nullptr;
+  int kind = 0;
+  if (SCAN && p.phase == 1 && seg > 0) kind = 2;
+  if (SCAN && (false || (p.phase == 2 && seg == 0))) return;
+  const bool last_range = jb + nchunks == nch_seq;
+  const float* s_in;
+  float* s_out;
+  if (!SCAN) {
+    s_in = jb == 0 ? (p.s0 ? p.s0 + sbase : nullptr) : carry;
+    s_out = last_range ? (p.s1 ? p.s1 + sbase : nullptr) : carry;
+  } else if (p.phase == 1) {
+    s_in = jb > 0 ? carry : (kind == 0 && p.s0 ? p.s0 + real : nullptr);
+    s_out = carry;
+  } else {
+    s_in = carry;
+    s_out = last_range && seg == p.segs - 1 && p.s1 ? p.s1 + real : nullptr;
+  }
+  const bool ident = SCAN && kind == 1 && jb == 0;  // the transition walk starts from I
+  const bool outputs = !SCAN || kind == 0;
+  if (nchunks == 0) {  // nothing in this range; a sequence with no tokens keeps its state
+    if (jb == 0 && nch_seq == 0 && s_out)
+      for (int i = tid; i < DIN * DIN; i += B_THREADS)
+        s_out[i] = ident ? (i / DIN == i % DIN ? 1.f : 0.f) : (s_in ? s_in[i] : 0.f);
+    return;
+  }
+  constexpr uint32_t kVBytes = (DIN / 64) * 8192u;
+  const int chain = n * H + h;
+  // The loads of chunk jb + j into buffer buf.  Fused: once stage 1 has
+  // published that record (false if it never does).
+  // seen: the record's ready flag as read earlier (fused)
+  auto ready_flag = [&](int j) { return ring.ready + chain * ring.ready_stride + (jb + j) % ring.R; };
+  auto issue_loads = [&](int j, int buf, int seen) -> bool {
+    const int jr = FUSED ? (jb + j) % ring.R : jb + j;
+    if (FUSED) {
+      if (!poll_at_least(ready_flag(j), jb + j + 1, seen)) return false;
+      fence_proxy_async_global();
+    }
+    const uint8_t* rec = p.records + ((size_t)(base + jr) * H + h) * REC_BYTES;
+    uint8_t* dst = sbp + (buf ? B_REC1 : B_REC0);
+    uint8_t* vdst = sbp + (buf ? B_V1 : B_V0);
+    mbar_arrive_expect_tx(&full[buf], REC_LOAD + (SCAN && kind == 1 ? 0u : kVBytes));
+    bulk_g2s(dst, rec, REC_LOAD, &full[buf]);
+    if (!SCAN || kind != 1) {
+#pragma unroll
+      for (int b = 0; b < DIN / 64; ++b)
+        tma_load_3d(vdst + b * 8192, &tm_v, &full[buf], b * 64, h, tok0 + CH * (jb + j));
+    }
+    return true;
+  };
+  // fused: the records of chunks below jb + upto are in shared memory (their
+  // copies have completed), so their slots are free for stage 1.  A relaxed
+  // store: nothing the chain still reads depends on it, and a release would
+  // wait for this thread's copies in flight.
+  auto release = [&](int upto) {
+    if (FUSED) st_relaxed_gpu(ring.consumed + chain * kFlagLine, jb + upto);
+  };
+  auto gamma_of = [&](int buf) {
+    return reinterpret_cast<const float*>(sbp + (buf ? B_REC1 : B_REC0) + REC_G);
+  };
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(mma_a, 1);
+    mbar_init(mma_b, 1);
+    mbar_init(&o_full[0], 1);
+    mbar_init(&o_full[1], 1);
+    mbar_init(&o_empty[0], B_OUTPUT);
+    mbar_init(&o_empty[1], B_OUTPUT);
+    mbar_init(st_ready, B_CHAIN);
+    mbar_init(ut_ready, B_CHAIN);
+    mbar_fence_init();
+    *s_abort = 0;
+    *s_range = 0;
+    if (!FUSED) {  // (fused: the issuer makes them, once stage 1 has published)
+      if (nchunks > 0) issue_loads(0, 0, 0);
+      if (nchunks > 1) issue_loads(1, 1, 0);
+    }
+  }
+  if (DIN == 64) {
+    for (uint32_t off = tid * 16; off < 8192; off += B_THREADS * 16) {
+      st_shared_v4(sb + B_V0 + 8192 + off, 0, 0, 0, 0);
+      st_shared_v4(sb + B_V1 + 8192 + off, 0, 0, 0, 0);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_base_s, TB_COLS);
+    if (!FUSED) tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  csync();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_base_s;
+  const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  const OperandLayout ST = kmajor(sb + B_ST, 16384);  // M = v, K = c
+  const OperandLayout UT = kmajor(sb + B_UT, 0);      // M = v, K = i
+  auto fail = [&]() {
+    *s_abort = 1;
+    set_status(6);
+  };
+
+  if (warp == B_THREADS / 32 - 1) {
+    // ---------------- issuer: one lane issues every MMA and every load
+    if ((tid & 31) == 0 && nchunks > 0) {
+      constexpr uint32_t ID_V = make_idesc(128, 64, true, false);                 // bf16
+      constexpr uint32_t ID_O2 = make_idesc(128, 64, false, true, true, true);    // fp16, -A
+      constexpr uint32_t ID_S = make_idesc(128, 128, false, false, false, true);  // fp16
+      // M3 of chunk j, U~^T = V^T (T diag beta)^T, needs no state: it is
+      // issued as soon as record j lands, ahead of the chain's own products.
+      auto issue_m3 = [&](int j) {
+        if (SCAN && kind == 1) return;  // no values: U~ = 0
+        const int b = j & 1;
+        const uint32_t rb = sb + (b ? B_REC1 : B_REC0), vb = sb + (b ? B_V1 : B_V0);
+        const uint64_t dva = layout_desc(mnmajor(vb, 8192), 0, 0);
+        const uint64_t dtb = layout_desc(kmajor(rb + REC_TB, 0), 0, 0);
+#pragma unroll
+        for (int k0 = 0; k0 < CH; k0 += 16)
+          umma_bf16(tmem + TB_UT + 64 * b, desc_adv(dva, k0, true), desc_adv(dtb, k0, false),
+                    ID_V, k0 > 0);
+      };
+      int issued = FUSED ? 0 : min(nchunks, 2), landed = 0;  // record loads issued / seen complete
+      int seen_next = 0;  // fused: the ready flag of the next load, read ahead
+      bool ok = true;
+      if (FUSED) {
+        ok = issue_loads(0, 0, ld_relaxed_gpu(ready_flag(0)));
+        issued = ok ? 1 : 0;
+        if (ok && nchunks > 1) {
+          ok = issue_loads(1, 1, ld_relaxed_gpu(ready_flag(1)));
+          issued += ok ? 1 : 0;
+        }
+      }
+      ok = ok && mbar_wait(&full[0], 0);
+      if (ok) {
+        landed = 1;
+        release(1);
+        tc_fence_after_sync();
+        issue_m3(0);
+      }
+      for (int j = 0; j < nchunks && ok; ++j) {
+        const int buf = j & 1, ob = j & 1;
+        const uint32_t rb = sb + (buf ? B_REC1 : B_REC0);
+        const uint32_t td = tmem + TB_D + 128 * ob;
+        if (!(ok = mbar_wait(st_ready, j & 1))) break;
+        if (j >= 2 && !(ok = mbar_wait(&o_empty[ob], ((j - 2) >> 1) & 1))) break;
+        tc_fence_after_sync();
+        {  // M4, D = -S^T W^T, alone (N = 64): the chain waits only for it.  The
+           // first half of M5, -S^T (q e^g)^T, follows into the next 64 columns
+           // and runs while the chain forms U^T.
+          const uint64_t dst = layout_desc(ST, 0, 0);
+          const uint64_t dw = layout_desc(mnmajor(rb + REC_WT, 16384), 0, 0);
+          const uint64_t dq = layout_desc(mnmajor(rb + REC_QT, 16384), 0, 0);
+#pragma unroll
+          for (int k0 = 0; k0 < DP; k0 += 16)
+            umma_bf16(td, desc_adv(dst, k0, false, 16384), desc_adv(dw, k0, true), ID_O2, k0 > 0);
+          umma_commit(mma_a);
+          // fused: read the ready flag of chunk j + 2 now; it is needed only
+          // once chunk j's products are done, and the load runs meanwhile
+          if (FUSED && j + 2 < nchunks) seen_next = ld_relaxed_gpu(ready_flag(j + 2));
+#pragma unroll
+          for (int k0 = 0; k0 < DP; k0 += 16)
+            umma_bf16(td + 64, desc_adv(dst, k0, false, 16384), desc_adv(dq, k0, true), ID_O2,
+                      k0 > 0);
+        }
+        if (!(ok = mbar_wait(ut_ready, j & 1))) break;
+        tc_fence_after_sync();
+        {
+          const uint64_t dut = layout_desc(UT, 0, 0);
+          const uint64_t daq = layout_desc(mnmajor(rb + REC_AQ, 8192), 0, 0);
+          const uint64_t dkb = layout_desc(kmajor(rb + REC_KBAR, 0), 0, 0);
+          // M6 first: the chain waits only for the state update; the second
+          // half of M5 (the output) runs while the chain rebuilds S^T
+#pragma unroll
+          for (int k0 = 0; k0 < CH; k0 += 16)
+            umma_bf16(tmem + TB_S, desc_adv(dut, k0, false), desc_adv(dkb, k0, false), ID_S, 1);
+          umma_commit(mma_b);
+#pragma unroll
+          for (int k0 = 0; k0 < CH; k0 += 16)
+            umma_bf16(td + 64, desc_adv(dut, k0, false), desc_adv(daq, k0, true), ID_O2, 1);
+          umma_commit(&o_full[ob]);
+        }
+        if (j + 2 < nchunks) {  // buffer buf is consumed once every product of chunk j is done
+          if (!(ok = mbar_wait(&o_full[ob], (j >> 1) & 1))) break;
+          fence_proxy_async_smem();
+          if (!(ok = issue_loads(j + 2, buf, seen_next))) break;
+          ++issued;
+        }
+        if (j + 1 < nchunks) {
+          if (!(ok = mbar_wait(&full[buf ^ 1], ((j + 1) >> 1) & 1))) break;
+          ++landed;
+          release(j + 2);
+          tc_fence_after_sync();
+          issue_m3(j + 1);
+        }
+      }
+      if (!ok) {
+        fail();
+        // let copies already issued land before the CTA's memory goes away
+        for (int r = landed; r < issued; ++r) mbar_wait(&full[r & 1], (r >> 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp >= B_CHAIN / 32) {
+    // ---------------- output warps: thread = value channel v, all 64 tokens
+    for (int j = 0; j < nchunks; ++j) {
+      const int ob = j & 1;
+      if (!mbar_wait(&o_full[ob], (j >> 1) & 1)) {
+        fail();
+        break;
+      }
+      tc_fence_after_sync();
+      const int valid = min(CH, len - CH * (jb + j));
+      float o[64];
+      tmem_ld64(tl + TB_D + 128 * ob + 64, o);  // holds -O^T
+      tc_fence_before_sync();
+      mbar_arrive(&o_empty[ob]);  // the TMEM tile may be overwritten now
+      if (v < DIN && p.out) {  // (no output buffer: a forward run for its states only)
+        OutT* out = static_cast<OutT*>(p.out) + (size_t)(tok0 + CH * (jb + j)) * H * DIN +
+                    (size_t)h * DIN + v;
+#pragma unroll
+        for (int r = 0; r < CH; ++r)
+          if (r < valid && (!SCAN || outputs)) store_out(out + (size_t)r * H * DIN, -p.scale * o[r]);
+      }
+    }
+  } else {
+    // ---------------- chain warps: decay, U^T and S^T operands, final state
+    // initial state: thread (v, half) holds S^T[v][64 half .. 64 half + 63]
+    const int c_lo = 64 * half;
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      float s0[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int c = c_lo + c0 + jj;
+        s0[jj] = ident ? (c == v && c < DIN ? 1.f : 0.f)
+                       : (s_in && c < DIN && v < DIN) ? s_in[(size_t)c * DIN + v] : 0.f;
+      }
+      tmem_st16(tl + TB_S + c_lo + c0, s0);
+      st8h(layout_addr(ST, v, c_lo + c0), s0);
+      st8h(layout_addr(ST, v, c_lo + c0 + 8), s0 + 8);
+    }
+    tmem_st_wait();
+    bool ok = true;
+    // A checkpoint due before chunk j is stored from the fp32 state that
+    // chunk's decay loads, while the tensor core runs: off the chain.
+    float* ck = nullptr;
+    for (int j = 0; j < nchunks; ++j) {
+      // invariant: ST = fp16(S_j) written by this thread; TMEM S = S_j
+      const int buf = j & 1, ob = j & 1;
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(st_ready);
+      if (!(ok = mbar_wait(&full[buf], (j >> 1) & 1))) break;
+      {  // decay the fp32 state by this chunk's e^{g_C} while the tensor core runs
+        const float* gam = gamma_of(buf);
+        float sv[64];
+        tmem_ld64(tl + TB_S + 64 * half, sv);
+        if (ck) {  // S[c][v] = S^T[v][c]
+#pragma unroll
+          for (int c0 = 0; c0 < 64; ++c0)
+            if (c_lo + c0 < DIN) ck[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+          ck = nullptr;
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float sd[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sd[jj] = sv[c0 + jj] * gam[64 * half + c0 + jj];
+          tmem_st16(tl + TB_S + 64 * half + c0, sd);
+        }
+        tmem_st_wait();
+      }
+      if (!(ok = mbar_wait(mma_a, j & 1))) break;
+      tc_fence_after_sync();
+      {  // U^T = U~^T - S^T W^T (fp16 operand): this thread's 32 tokens
+        float u[32], w[32];
+        const uint32_t tu = tl + TB_UT + 64 * buf + 32 * half, tw = tl + TB_D + 128 * ob + 32 * half;
+        tmem_ld16(tu, *reinterpret_cast<float(*)[16]>(u));
+        tmem_ld16(tu + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+        tmem_ld16(tw, *reinterpret_cast<float(*)[16]>(w));
+        tmem_ld16(tw + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+        tmem_ld_wait();
+        if (SCAN && kind == 1) {  // no values: U = -S W^T alone
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = w[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] += w[i];
+        }
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(ut_ready);
+      if (!(ok = mbar_wait(mma_b, j & 1))) break;
+      tc_fence_after_sync();
+      {  // the fp16 state operand for the next chunk (and the final state)
+        float sv[64];
+        tmem_ld64(tl + TB_S + 64 * half, sv);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 8) st8h(layout_addr(ST, v, c_lo + c0), sv + c0);
+        if (j + 1 == nchunks && s_out && v < DIN) {  // S[c][v] = S^T[v][c]
+#pragma unroll
+          for (int c0 = 0; c0 < 64; ++c0)
+            if (c_lo + c0 < DIN) s_out[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+        }
+        const int done = jb + j + 1;  // chunks of the sequence finished
+        if (p.ckpt && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.n_ckpt && v < DIN) {
+          float* cp = p.ckpt + ((size_t)(n * p.n_ckpt + done / p.ckpt_every - 1) * H + h) * DIN * DIN;
+          if (j + 1 < nchunks) {
+            ck = cp;  // with the next chunk's decay
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; ++c0)
+              if (c_lo + c0 < DIN) cp[(size_t)(c_lo + c0) * DIN + v] = sv[c0];
+          }
+        }
+      }
+    }
+    if (!ok) {
+      fail();
+    } else {
+      // An fp16 operand that overflowed (a state entry or a correction u
+      // beyond the fp16 range) turns into inf / NaN in every later state, so
+      // one check of the range's last state, after the chain, catches it.
+      float sv[64];
+      tmem_ld64(tl + TB_S + 64 * half, sv);
+      bool in_range = true;
+#pragma unroll
+      for (int c0 = 0; c0 < 64; ++c0) in_range &= fabsf(sv[c0]) <= kOperandMax;
+      if (!in_range) *s_range = 1;
+    }
+  }
+  tc_fence_before_sync();
+  csync();
+  if (tid == 0 && *s_range) set_status(8);
+  if (warp == 0) tmem_dealloc(tmem, TB_COLS);
+}
+
+// The whole prefill of fixed-length sequences in one cooperative launch of
+// one CTA per SM (see FusedRing): CTA c < B H walks chain c with its first
+// B_THREADS threads, every other CTA runs two stage-1 bodies, one per
+// 256-thread half, on its two halves of shared memory and tensor memory.
+template <int DIN, typename OutT>
+__global__ void __launch_bounds__(F_THREADS, 1)
+    kda_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ IntraParams ip, const __grid_constant__ StateParams sp,
+                     const __grid_constant__ FusedRing ring) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((int)blockIdx.x < sp.n_seq * sp.H) {
+    if (threadIdx.x < B_THREADS)
+      fused_state_body<DIN, OutT>(tm_v, sp, ring, smem_raw, threadIdx.x, (int)blockIdx.x / sp.H,
+                                  (int)blockIdx.x % sp.H);
+    return;
+  }
+  const int part = threadIdx.x / A_THREADS;
+  intra_body<DIN, false, false, true, const IntraParams&>(tm_q, tm_k, tm_g, ip, ring,
+                                                          smem_raw + part * A_SMEM,
+                                                          threadIdx.x % A_THREADS, 1 + part);
+}
+
 // Packed sequences: the plan every later kernel reads instead of cu_seqlens,
 //   plan[n]             = sum_{m < n} ceil(len_m / 64)   (n = 0..N, record offsets)
 //   plan[N + 1 + n]     = start_n,   plan[2N + 1 + n] = len_n   (n < N)
@@ -1480,6 +2039,28 @@ int ring_segment_chunks(int nc_max, int chains) {
   return (int)std::max<long long>(32, seg);
 }
 
+// Records per chain in the fused launch's ring (at most the chunks of a
+// sequence): 16 chunks x 32 heads x 65 KB is 33 MB, well inside L2.
+constexpr int kFusedRing = 16;
+// KDA_SCHEDULE=rounds, read on every call, keeps fixed-length calls on the
+// two-kernel round schedule instead of the fused launch (for comparisons).
+bool rounds_forced() {
+  const char* e = std::getenv("KDA_SCHEDULE");
+  return e && std::strcmp(e, "rounds") == 0;
+}
+// Where the fused launch is the faster schedule (measured on the fixed-length
+// prefill, d = 128, against the round schedule): its chains run about as
+// fast as the plain state pass, but its stage 1, on the SMs the chains leave
+// and with each record's publication to pay for, keeps up with them only
+// while they are few.  With up to sms / 9 chains (16 of 152 SMs) it wins at
+// every length tried (up to 64k tokens, 4-10 % from 8k on); with up to sms /
+// 4 (32 heads) it wins up to 512 chunks (8-25 %) and loses 1 % at 1024; with
+// 64 chains it loses 25-50 %.
+bool use_fused(bool eligible, int chains, int nc, int sms) {
+  return eligible && !rounds_forced() &&
+         (9 * chains <= sms || (4 * chains <= sms && nc <= 512));
+}
+
 // The overlapped schedule pays off for sequences of at least 128 chunks
 // (8192 tokens) and few long-lived state chains: stage 2 must leave stage 1
 // at least half the SMs.
@@ -1572,6 +2153,63 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // longest length (short sequences' chains end early and give their SMs back).
   // A segment scan walks 2 segs - 1 chains per (sequence, head); its state
   // passes are short, so they may take up to every SM.
+  // The fused single launch (kda_fused_kernel): fixed lengths, no scan, no
+  // per-round host copies, not the ablation, with the workspace's counters,
+  // where it is the faster schedule (use_fused).  Its ring of records stays
+  // in L2.
+  if (use_fused(!pr.cu_seqlens && segs == 1 && !pr.hooks && !pr.diag_per_pair && allow_overlap &&
+                    carry && grid_done,
+                pr.n_seq * pr.H, nc_max, sms)) {
+    const int chains = pr.n_seq * pr.H, R = std::min(kFusedRing, nc_max);
+    // flags in the carry (not used by this path): the counter's line, a line
+    // per chain for consumed, then each chain's ready slots on lines of their own
+    const int ready_stride = (R + kFlagLine - 1) / kFlagLine * kFlagLine;
+    int* flags = reinterpret_cast<int*>(carry);
+    const FusedRing fr{flags + (size_t)(1 + chains) * kFlagLine, flags + kFlagLine, flags, R,
+                       ready_stride};
+    const size_t flag_ints = (size_t)(1 + chains) * kFlagLine + (size_t)chains * ready_stride;
+    e = cudaMemsetAsync(flags, 0, flag_ints * sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+    IntraParams ip{};
+    ip.beta = static_cast<const __nv_bfloat16*>(pr.beta);
+    ip.records = records;
+    ip.T = pr.T;
+    ip.n_seq = pr.n_seq;
+    ip.H = pr.H;
+    ip.check_decay = pr.check_decay ? 1 : 0;
+    ip.j_lo = 0;
+    ip.seg_len = nc_max;
+    ip.n_items = nc_max * chains;
+    StateParams sp{};
+    sp.records = records;
+    sp.s0 = pr.initial_state;
+    sp.s1 = pr.final_state;
+    sp.out = pr.out;
+    sp.T = pr.T;
+    sp.n_seq = pr.n_seq;
+    sp.H = pr.H;
+    sp.j_lo = 0;
+    sp.j_hi = nc_max;
+    sp.scale = pr.scale;
+    sp.ckpt = pr.ckpt;
+    sp.ckpt_every = pr.ckpt_every_chunks;
+    sp.n_ckpt = pr.n_ckpt;
+    sp.segs = 1;
+    const auto fused = kda_fused_kernel<DIN, OutT>;
+    e = set_smem(fused, F_SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(F_THREADS);
+    cfg.dynamicSmemBytes = F_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused, tq, tk, tg, tv, ip, sp, fr);
+  }
   const int long_chains = segs > 1 ? (pr.n_seq / segs) * (2 * segs - 1) * pr.H
       : pr.cu_seqlens ? pr.H * (int)(((long long)pr.T_total + pr.T - 1) / std::max(pr.T, 1))
       : pr.n_seq * pr.H;
@@ -1642,6 +2280,7 @@ int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {
   int nc_max = (max_len + CH - 1) / CH;
   if (n_seq <= 0 || nc_max <= 0 || H <= 0) return 0;
   const int segs = packed ? 1 : scan_segments(n_seq, max_len, H, sms, 0);
+  if (use_fused(!packed && segs == 1, n_seq * H, nc_max, sms)) return 1;
   int plan = packed ? 1 : 0, chains = n_seq * H, tail = 0;
   if (segs > 1) {  // plan, the walks, combine, second walks
     nc_max = (nc_max + segs - 1) / segs;

@@ -1,10 +1,17 @@
-"""The overlapped (segmented) prefill schedule: sequences of at least 128
-chunks with few (sequence, head) states run as segments whose intra-chunk
-stage overlaps the previous segment's state pass, with the state carried
-between segments.  Every variant of that path is checked against the fp64
-oracle: several sequences, packed sequences of unequal length (some shorter
-than a segment, one empty), bf16 output, d = 64, an in-place state and the
-per-pair diagonal ablation."""
+"""The two schedules of a long prefill with few (sequence, head) states.
+
+* Fused (fixed lengths, the default): one cooperative launch in which some
+  CTAs walk the state chains while the others run the intra-chunk stage in
+  chunk order into a ring of records.
+* Rounds (packed sequences, the ablation, host-buffer calls, or
+  KDA_SCHEDULE=rounds): segments whose intra-chunk stage overlaps the
+  previous segment's state pass, with the state carried between segments.
+
+Every variant is checked against the fp64 oracle under both schedules where
+both apply: several sequences, packed sequences of unequal length (some
+shorter than a segment, one empty), bf16 output, d = 64, an in-place state
+and the per-pair diagonal ablation; and the two schedules agree bit for bit.
+"""
 import pytest
 import torch
 
@@ -30,16 +37,52 @@ def _ref(x, **kw):
                               x["initial_state"], **kw)
 
 
-def test_schedule_is_segmented():
-    # the cases below only test what they claim if these shapes take the
-    # segmented schedule (2 launches per segment) and short ones do not
+@pytest.fixture(params=["fused", "rounds"])
+def schedule(request, monkeypatch):
+    if request.param == "rounds":
+        monkeypatch.setenv("KDA_SCHEDULE", "rounds")
+    else:
+        monkeypatch.delenv("KDA_SCHEDULE", raising=False)
+    return request.param
+
+
+def test_schedules(monkeypatch):
+    # the cases below only test what they claim if these fixed-length shapes
+    # take one fused launch (few chains; 32 of them up to 512 chunks), the
+    # 32-head 64k problem the segmented schedule, and with
+    # KDA_SCHEDULE=rounds every shape the segmented schedule (2 launches per
+    # segment) from 128 chunks on
+    monkeypatch.delenv("KDA_SCHEDULE", raising=False)
+    for shape in ((2, 9000, 2), (1, 8192, 32), (1, 4096, 2), (1, 65536, 16)):
+        assert binding.kda_chunk_fwd_launches(*shape) == 1
+    assert binding.kda_chunk_fwd_launches(1, 65536, 32) > 2
+    monkeypatch.setenv("KDA_SCHEDULE", "rounds")
     assert binding.kda_chunk_fwd_launches(2, 9000, 2) > 2
     assert binding.kda_chunk_fwd_launches(1, 8192, 32) > 2
     assert binding.kda_chunk_fwd_launches(1, 4096, 2) == 2
 
 
 @pytest.mark.parametrize("d,out_dtype", [(128, torch.float32), (64, torch.bfloat16)])
-def test_overlap_batch_of_sequences(d, out_dtype):
+def test_fused_equals_rounds(monkeypatch, d, out_dtype):
+    """The same arithmetic per item and per chunk under either schedule."""
+    x = gen.make_inputs(2, 9000, 2, d, d, seed=46, init_std=0.02)
+    g = _cuda(x)
+    res = []
+    for sched in ("fused", "rounds"):
+        if sched == "rounds":
+            monkeypatch.setenv("KDA_SCHEDULE", "rounds")
+        else:
+            monkeypatch.delenv("KDA_SCHEDULE", raising=False)
+        out, fin = binding.kda_chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
+                                         g["initial_state"], scale=0.9, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        assert binding.kda_last_device_status() == 0
+        res.append((out, fin))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+@pytest.mark.parametrize("d,out_dtype", [(128, torch.float32), (64, torch.bfloat16)])
+def test_overlap_batch_of_sequences(schedule, d, out_dtype):
     x = gen.make_inputs(2, 9000, 2, d, d, seed=41, init_std=0.02)
     g = _cuda(x)
     out, fin = binding.kda_chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
@@ -54,7 +97,7 @@ def test_overlap_batch_of_sequences(d, out_dtype):
     assert_state_close(fin, rs)
 
 
-def test_overlap_in_place_state():
+def test_overlap_in_place_state(schedule):
     x = gen.make_inputs(1, 8300, 2, 128, 128, seed=42, init_std=0.02)
     g = _cuda(x)
     s = g["initial_state"].clone()
@@ -94,8 +137,8 @@ def test_overlap_diag_per_pair_ablation(monkeypatch):
     assert_state_close(fin, rs)
 
 
-def test_overlap_repeated_calls_are_identical():
-    """The finished-CTA counter resets itself: back-to-back calls agree bit for bit."""
+def test_overlap_repeated_calls_are_identical(schedule):
+    """The item counters and ring flags start over: back-to-back calls agree bit for bit."""
     x = gen.make_inputs(1, 8192, 2, 128, 128, seed=45, init_std=0.02)
     g = _cuda(x)
     outs = []

@@ -6,8 +6,10 @@ finished), so its workspace stops growing with T.
 * The workspace of T = 65536 and of T = 122880 at 64 heads (both without
   the segment scan, both overlapped, 4.4 and 8.2 GB of records if kept
   whole) is the same, and under 1 GB.
-* The T = 65536, 64-head call, whose ring wraps four times, meets the oracle
-  bar on every output and final-state element, and equals the same call made
+* The T = 65536, 64-head call on the round schedule (the default for this
+  many chains, and forced here with KDA_SCHEDULE=rounds), whose ring wraps
+  four times, meets the oracle bar on every output and final-state element,
+  and equals bit for bit the same call made through the default entry and
   through the one-segment entry point.
 """
 import pytest
@@ -36,13 +38,20 @@ def test_workspace_does_not_grow_with_T():
     assert a < 1 << 30
 
 
-def test_ring_that_wraps_against_oracle():
+def test_ring_that_wraps_against_oracle(monkeypatch):
     x = gen.make_inputs(1, 65536, 64, 128, 128, seed=71, init_std=0.02)
     g = {k: v.cuda() for k, v in x.items()}
+    monkeypatch.setenv("KDA_SCHEDULE", "rounds")
     out, fin = binding.kda_chunk_fwd(*[g[k] for k in KEYS], g["initial_state"])
     torch.cuda.synchronize()
     assert binding.kda_last_device_status() == 0
-    # the one-segment entry point makes the same call
+    monkeypatch.delenv("KDA_SCHEDULE")
+    # the default entry, and the one-segment entry point, make the same call
+    out2, fin2 = binding.kda_chunk_fwd(*[g[k] for k in KEYS], g["initial_state"])
+    torch.cuda.synchronize()
+    assert binding.kda_last_device_status() == 0
+    assert torch.equal(out, out2) and torch.equal(fin, fin2)
+    del out2, fin2
     out2, fin2 = binding.kda_chunk_fwd_segments(*[g[k] for k in KEYS], g["initial_state"],
                                                 n_segments=1)
     torch.cuda.synchronize()

@@ -90,8 +90,8 @@ def test_segments_close_to_unsegmented():
 
 def test_long_sequences_with_few_heads_take_the_scan():
     """kda_chunk_fwd chooses the scan for the 1M-token, 16-head problem but not
-    for the 64k, 32-head one.  A fixed-length call launches two kernels per
-    round of its schedule; a scan adds its plan, combine and second-walk
-    kernels, so its count is odd."""
+    for the 64k, 32-head one.  Without the scan that call launches two
+    kernels per round of its schedule; a scan adds its plan, combine and
+    second-walk kernels, so its count is odd."""
     assert binding.kda_chunk_fwd_launches(1, 1 << 20, 16) % 2 == 1
     assert binding.kda_chunk_fwd_launches(1, 1 << 16, 32) % 2 == 0
