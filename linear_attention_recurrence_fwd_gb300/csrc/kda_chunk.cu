@@ -655,7 +655,8 @@ __device__ __forceinline__ void intra_body(const CUtensorMap& tm_q, const CUtens
   // The bytes and the flag reach L2 by different paths, so the flag is a
   // release at GPU scope: a chain that sees it finds the bytes there.  Every
   // record is published before its body can wait for a ring slot, so no
-  // record waits behind another chain's progress.
+  // record waits behind another chain's progress.  (Publishing two records
+  // per release, or from another thread after a barrier, measured slower.)
   auto publish = [&]() {  // thread 0
     bulk_wait_all();
     fence_proxy_async_global();
@@ -893,8 +894,9 @@ __device__ __forceinline__ void intra_body(const CUtensorMap& tm_q, const CUtens
     csync();
     if (tid == 0) {  // q e^g, K-bar and A_qk are final: store them while the solve runs
       // fused: the slot's previous record (chunk - R) must have been copied in
-      const bool slot_free = !FUSED || poll_at_least(ring.consumed + cur.chain * kFlagLine,
-                                                     cur.chunk - ring.R + 1, consumed_seen, true);
+      const int need = cur.chunk - ring.R + 1;
+      const bool slot_free = !FUSED || poll_at_least(ring.consumed + cur.chain * kFlagLine, need,
+                                                     consumed_seen, true);
       if (slot_free) {
         if (FUSED) fence_proxy_async_global();
         bulk_s2g(rec + REC_QT, sb + A_STG + REC_QT, REC_TB - REC_QT);
@@ -2042,11 +2044,16 @@ int ring_segment_chunks(int nc_max, int chains) {
 // Records per chain in the fused launch's ring (at most the chunks of a
 // sequence): 16 chunks x 32 heads x 65 KB is 33 MB, well inside L2.
 constexpr int kFusedRing = 16;
-// KDA_SCHEDULE=rounds, read on every call, keeps fixed-length calls on the
-// two-kernel round schedule instead of the fused launch (for comparisons).
-bool rounds_forced() {
+// KDA_SCHEDULE, read on every call, overrides the choice below for
+// comparisons: "rounds" keeps fixed-length calls on the two-kernel round
+// schedule, "fused" takes the fused launch wherever it can run (chains on at
+// most half the SMs).  Returns 'r', 'f' or 0.
+char schedule_forced() {
   const char* e = std::getenv("KDA_SCHEDULE");
-  return e && std::strcmp(e, "rounds") == 0;
+  if (!e) return 0;
+  if (std::strcmp(e, "rounds") == 0) return 'r';
+  if (std::strcmp(e, "fused") == 0) return 'f';
+  return 0;
 }
 // Where the fused launch is the faster schedule (measured on the fixed-length
 // prefill, d = 128, against the round schedule): its chains run about as
@@ -2057,8 +2064,10 @@ bool rounds_forced() {
 // 4 (32 heads) it wins up to 512 chunks (8-25 %) and loses 1 % at 1024; with
 // 64 chains it loses 25-50 %.
 bool use_fused(bool eligible, int chains, int nc, int sms) {
-  return eligible && !rounds_forced() &&
-         (9 * chains <= sms || (4 * chains <= sms && nc <= 512));
+  const char f = schedule_forced();
+  if (!eligible || f == 'r') return false;
+  if (f == 'f') return 2 * chains <= sms;
+  return 9 * chains <= sms || (4 * chains <= sms && nc <= 512);
 }
 
 // The overlapped schedule pays off for sequences of at least 128 chunks

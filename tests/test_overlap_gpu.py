@@ -62,15 +62,24 @@ def test_schedules(monkeypatch):
     assert binding.kda_chunk_fwd_launches(1, 4096, 2) == 2
 
 
-@pytest.mark.parametrize("d,out_dtype", [(128, torch.float32), (64, torch.bfloat16)])
-def test_fused_equals_rounds(monkeypatch, d, out_dtype):
-    """The same arithmetic per item and per chunk under either schedule."""
-    x = gen.make_inputs(2, 9000, 2, d, d, seed=46, init_std=0.02)
+@pytest.mark.parametrize("d,out_dtype,B,T,H,forced", [(128, torch.float32, 2, 9000, 2, "auto"),
+                                                      (64, torch.bfloat16, 2, 9000, 2, "auto"),
+                                                      (128, torch.float32, 1, 8192, 64, "fused")])
+def test_fused_equals_rounds(monkeypatch, d, out_dtype, B, T, H, forced):
+    """The same arithmetic per item and per chunk under either schedule (64
+    chains: a fused launch that KDA_SCHEDULE=fused forces, half the SMs on
+    chains)."""
+    if forced == "fused":
+        monkeypatch.setenv("KDA_SCHEDULE", "fused")
+        assert binding.kda_chunk_fwd_launches(B, T, H) == 1
+    x = gen.make_inputs(B, T, H, d, d, seed=46, init_std=0.02)
     g = _cuda(x)
     res = []
     for sched in ("fused", "rounds"):
         if sched == "rounds":
             monkeypatch.setenv("KDA_SCHEDULE", "rounds")
+        elif forced == "fused":
+            monkeypatch.setenv("KDA_SCHEDULE", "fused")
         else:
             monkeypatch.delenv("KDA_SCHEDULE", raising=False)
         out, fin = binding.kda_chunk_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"],
