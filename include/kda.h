@@ -37,6 +37,14 @@
  *     that needs no bound on the decay, instead of with the dense
  *     tensor-core products.  Results agree within rounding; it exists to
  *     measure what the bound saves.
+ *   - Schedule.  kda_chunk_fwd runs a fixed-length prefill either as rounds
+ *     of two kernels (an intra-chunk stage, then the state pass) or, for few
+ *     (sequence, head) chains, as one cooperative launch that runs both and
+ *     keeps the per-chunk records in a small ring; it picks the one measured
+ *     faster for the shape.  KDA_SCHEDULE=rounds or KDA_SCHEDULE=fused in
+ *     the environment (read on every call) forces one (fused where it can
+ *     run: chains on at most half the SMs).  Results are the same bit for
+ *     bit either way.
  *   - Supported head dims: d_k = d_v = 128, and d_k = d_v = 64 (prefill
  *     only).  Others return KDA_ERR_UNSUPPORTED.
  *   - Range.  The prefill entry points carry the state in fp32 but feed
@@ -252,9 +260,11 @@ KDA_API kda_status_t kda_chunk_bwd(const void* q, const void* k, const void* v,
 KDA_API size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int d_k, int d_v);
 
 /* Kernel launches one kda_chunk_fwd call of this shape makes on the current
- * device (the schedule depends on the device's SM count): 2 for the plain
- * two-stage schedule, 2 per segment for the overlapped one.  -1 on a bad
- * argument or a CUDA error.  A diagnostic for profiling and benchmarks. */
+ * device (the schedule depends on the device's SM count and on
+ * KDA_SCHEDULE): 1 for the fused launch, 2 for the plain two-stage
+ * schedule, 2 per segment for the overlapped one, more with the segment
+ * scan.  -1 on a bad argument or a CUDA error.  A diagnostic for profiling
+ * and benchmarks. */
 KDA_API int kda_chunk_fwd_launches(int B, int T, int H);
 
 /*
