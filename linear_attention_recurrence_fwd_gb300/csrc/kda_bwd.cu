@@ -14,16 +14,20 @@
 //   G    = Diag(alpha_t) dS'                  (gradient of S_{t-1}).
 //
 // Layout of the work: the forward (the chunked tensor-core path) saves the
-// state at every chunk boundary; one CTA per (sequence, head, block of 8
-// value columns) then walks the chunks from last to first.  For each chunk
-// it recomputes the 64 token states in fp32 from the saved chunk-start state
-// (S'_t to a per-CTA scratch in global memory, u_t and w_t to shared
-// memory), then runs the reverse recurrence above over the chunk's tokens.
-// Thread c holds row c of G for the block's columns in registers: dot
-// products along a row stay in the thread, sums down a column (w and du)
-// take a warp reduce-scatter and one pass over shared memory.  This is
-// CUDA-core work, serial in tokens per (sequence, head): a first, exact
-// formulation, not a tensor-core one.
+// state at every chunk boundary and, where it can (the fused launch), every
+// token's u; one CTA per (sequence, head, block of 8 value columns) then
+// walks the chunks from last to first.  For each chunk it rebuilds the token
+// states in fp32 from the saved chunk-start state: with u given that is a
+// local step per token (S'_t = Diag(alpha_t) S_{t-1}, S_t = S'_t + k_t u_t^T,
+// w_t = u_t / beta_t), and only without it, or for a token with beta = 0,
+// does w take a column sum.  It keeps the state before every 4th token (in a
+// per-CTA scratch in global memory) and, in the reverse recurrence, rebuilds
+// each group of 4 token states in registers from it.  Thread c holds row c of
+// G for the block's columns in registers: dot products along a row stay in
+// the thread, sums down a column (du, and w without u) take a warp
+// reduce-scatter and one pass over shared memory.  This is CUDA-core work,
+// serial in tokens per (sequence, head): an exact token-level formulation,
+// not a tensor-core one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,7 +48,8 @@ struct BwdParams {
   const float* dout;  // [B][T][H][d]
   const float* dfin;  // [B][H][d][d] or null (zeros)
   float *dq, *dk, *dv, *dla, *dbeta, *ds0;
-  float* scratch;  // [B * H][64][d][d]
+  float* scratch;      // [B * H][64 / SUB][d][d]
+  const float* u_fwd;  // [B][T][H][d]: every token's u from the forward (HAVE_U), or null
   int T, H, n_ckpt;
   float scale;
 };
@@ -55,6 +60,10 @@ struct BwdParams {
 // the blocks, by atomic adds into zeroed buffers.  Thread c owns key row c
 // and the block's CB columns.
 constexpr int CB = 8;
+// Tokens per sub-block of the reverse pass: the state before each sub-block
+// is saved (in the per-CTA scratch), and the sub-block's token states are
+// rebuilt in registers when the reverse pass reaches it.
+constexpr int SUB = 4;
 
 template <int DIN>
 struct BwdShape {
@@ -107,7 +116,10 @@ __device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int 
   if ((lane & ((1 << LOW) - 1)) == 0) red[warp * CB + (lane >> LOW)] = x[0];
 }
 
-template <int DIN>
+// HAVE_U: the forward left every token's u, so the chunk's token states
+// follow from the saved chunk-start state with no column sums (w = u / beta;
+// only a token with beta = 0 takes the sum for its w).
+template <int DIN, bool HAVE_U>
 __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdParams p) {
   using S = BwdShape<DIN>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -129,8 +141,9 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
   const size_t dd = (size_t)DIN * DIN;
   const size_t plane = ((size_t)n * H + h) * dd;     // this (sequence, head) in [B][H][d][d]
   const size_t row = plane + (size_t)c * DIN + vb;  // element (c, vb)
-  // per-thread scratch of one chunk's S'_t: token i, this thread's CB values
-  float* scratch = p.scratch + (((size_t)n * H + h) * S::BLOCKS + blk) * BW_CH * DIN * CB +
+  // per-thread scratch of one chunk: the state before each sub-block, this
+  // thread's CB values
+  float* scratch = p.scratch + (((size_t)n * H + h) * S::BLOCKS + blk) * (BW_CH / SUB) * DIN * CB +
                    (size_t)tid * CB;
 
   auto load_row = [&](const float* src, float (&x)[CB]) {  // x = src[c][vb .. vb + CB)
@@ -170,11 +183,16 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
       if (i < L) z = *reinterpret_cast<const uint4*>(p.v + (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c8);
       *reinterpret_cast<uint4*>(sv + i * CB + c8) = z;
     }
-    for (int e = tid; e < BW_CH * CB / 4; e += S::THREADS) {  // the block's do columns
+    for (int e = tid; e < BW_CH * CB / 4; e += S::THREADS) {  // the block's do (and u) columns
       const int i = e / (CB / 4), c4 = (e % (CB / 4)) * 4;
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < L) z = *reinterpret_cast<const float4*>(p.dout + (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c4);
+      const size_t off = (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c4;
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f), zu = z;
+      if (i < L) {
+        z = *reinterpret_cast<const float4*>(p.dout + off);
+        if (HAVE_U) zu = *reinterpret_cast<const float4*>(p.u_fwd + off);
+      }
       *reinterpret_cast<float4*>(sdo + i * CB + c4) = z;
+      if (HAVE_U) *reinterpret_cast<float4*>(su + i * CB + c4) = zu;
     }
     if (tid < BW_CH) sbeta[tid] = tid < L ? bfv(p.beta, ((size_t)n * T + t0 + tid) * H + h) : 0.f;
     __syncthreads();
@@ -189,37 +207,76 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
     for (int i = 0; i < L; ++i) {
       const float a = __expf(__bfloat162float(sla[i * DIN + c]));
       const float kc = __bfloat162float(sk[i * DIN + c]);
+      if ((i & (SUB - 1)) == 0) {  // S_{t-1}: the state before this sub-block
+        float* dst = scratch + (size_t)(i / SUB) * DIN * CB;
+#pragma unroll
+        for (int j = 0; j < CB; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+      }
       float x[CB];
 #pragma unroll
       for (int j = 0; j < CB; ++j) {
         s[j] *= a;  // S'_t
         x[j] = s[j] * kc;
       }
-      float* dst = scratch + (size_t)i * DIN * CB;
+      const float b = sbeta[i];
+      if (!HAVE_U || b == 0.f) {  // (with u given: the same for every thread)
+        column_partials(x, red, warp, lane);
+        __syncthreads();
+        if (tid < CB) {  // w = v - S'^T k, u = beta w
+          float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < CB; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-      column_partials(x, red, warp, lane);
-      __syncthreads();
-      if (tid < CB) {  // w = v - S'^T k, u = beta w
-        float acc = 0.f;
-#pragma unroll
-        for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * CB + tid];
-        const float w = __bfloat162float(sv[i * CB + tid]) - acc;
-        sw[i * CB + tid] = w;
-        su[i * CB + tid] = sbeta[i] * w;
+          for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * CB + tid];
+          const float w = __bfloat162float(sv[i * CB + tid]) - acc;
+          sw[i * CB + tid] = w;
+          su[i * CB + tid] = b * w;
+        }
+        __syncthreads();
       }
-      __syncthreads();
 #pragma unroll
       for (int j = 0; j < CB; ++j) s[j] += kc * su[i * CB + j];  // S_t
     }
+    if (HAVE_U) {  // w = u / beta where beta != 0
+      for (int e = tid; e < L * CB; e += S::THREADS) {
+        const float b = sbeta[e / CB];
+        if (b != 0.f) sw[e] = su[e] / b;
+      }
+      __syncthreads();
+    }
 
-    // ---- the reverse recurrence over the chunk's tokens
-    for (int i = L - 1; i >= 0; --i) {
+    // ---- the reverse recurrence over the chunk's tokens, SUB at a time: the
+    // sub-block's S'_t are rebuilt in registers from the state saved before
+    // it (a local step per token: u is known), whose load is issued one
+    // sub-block ahead.
+    const int nsub = (L + SUB - 1) / SUB;
+    float nxt[CB];
+    if (nsub > 0) load_row(scratch + (size_t)(nsub - 1) * DIN * CB, nxt);
+    for (int sbk = nsub - 1; sbk >= 0; --sbk) {
+      float spq[SUB][CB];
+      {
+        float st[CB];
+#pragma unroll
+        for (int j = 0; j < CB; ++j) st[j] = nxt[j];
+        if (sbk > 0) load_row(scratch + (size_t)(sbk - 1) * DIN * CB, nxt);
+#pragma unroll
+        for (int q = 0; q < SUB; ++q) {
+          const int i = SUB * sbk + q;
+          const float a = i < L ? __expf(__bfloat162float(sla[i * DIN + c])) : 1.f;
+          const float kc = i < L ? __bfloat162float(sk[i * DIN + c]) : 0.f;
+#pragma unroll
+          for (int j = 0; j < CB; ++j) {
+            st[j] *= a;
+            spq[q][j] = st[j];
+            st[j] += kc * su[(i < L ? i : 0) * CB + j];
+          }
+        }
+      }
+#pragma unroll
+    for (int q = SUB - 1; q >= 0; --q) {
+      const int i = SUB * sbk + q;
+      if (i >= L) continue;  // (the same for every thread)
       const size_t tok = ((size_t)n * T + t0 + i) * H + h;
-      // S'_t, read back from this thread's scratch; the load overlaps the
-      // column sum below, which does not need it
-      float sp[CB];
-      load_row(scratch + (size_t)i * DIN * CB, sp);
+      const float* sp = spq[q];
       const float qc = __bfloat162float(sq[i * DIN + c]);
       const float kc = __bfloat162float(sk[i * DIN + c]);
       const float a = __expf(__bfloat162float(sla[i * DIN + c]));
@@ -265,6 +322,7 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
       atomicAdd(p.dk + tok * DIN + c, xk);
       atomicAdd(p.dla + tok * DIN + c, xa);
     }
+    }
   }
   if (p.ds0) {
 #pragma unroll
@@ -273,14 +331,20 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
   }
 }
 
-template <int DIN>
+template <int DIN, bool HAVE_U>
 cudaError_t launch_bwd_kernel(const BwdParams& bp, int B, int H, cudaStream_t stream) {
   using S = BwdShape<DIN>;
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_kernel<DIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)S::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_kernel<DIN, HAVE_U>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
   if (e != cudaSuccess) return e;
-  kda_bwd_kernel<DIN><<<dim3((unsigned)H, (unsigned)B, S::BLOCKS), S::THREADS, S::SMEM, stream>>>(bp);
+  kda_bwd_kernel<DIN, HAVE_U>
+      <<<dim3((unsigned)H, (unsigned)B, S::BLOCKS), S::THREADS, S::SMEM, stream>>>(bp);
   return cudaGetLastError();
+}
+template <int DIN>
+cudaError_t launch_bwd_kernel(const BwdParams& bp, int B, int H, cudaStream_t stream) {
+  return bp.u_fwd ? launch_bwd_kernel<DIN, true>(bp, B, H, stream)
+                  : launch_bwd_kernel<DIN, false>(bp, B, H, stream);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -288,12 +352,13 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
 
 // Workspace of the backward: the forward's own workspace, the state at every
-// chunk boundary, and the per-(sequence, head) scratch of one chunk's states.
+// chunk boundary, the per-(sequence, head) scratch of one chunk's sub-block
+// states, and every token's u from the forward (fp32, like an output).
 size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d) {
   const size_t dd = (size_t)d * d * sizeof(float);
   const size_t n_ckpt = (size_t)(T / BW_CH);
   return align256(chunk_workspace_bytes(false, B, T, H)) + align256((size_t)B * n_ckpt * H * dd) +
-         align256((size_t)B * H * BW_CH * dd);
+         align256((size_t)B * H * (BW_CH / SUB) * dd) + align256((size_t)B * T * H * d * sizeof(float));
 }
 
 cudaError_t launch_chunk_bwd(const ChunkProblem& fwd, const float* d_out, const float* d_final,
@@ -307,6 +372,8 @@ cudaError_t launch_chunk_bwd(const ChunkProblem& fwd, const float* d_out, const 
   float* ckpt = reinterpret_cast<float*>(ws + align256(chunk_workspace_bytes(false, B, T, H)));
   float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ckpt) +
                                             align256((size_t)B * n_ckpt * H * dd));
+  float* ufwd = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) +
+                                         align256((size_t)B * H * (BW_CH / SUB) * dd));
   // the forward, for the state at every chunk boundary (its outputs are not needed)
   ChunkProblem f = fwd;
   f.out = nullptr;
@@ -315,12 +382,15 @@ cudaError_t launch_chunk_bwd(const ChunkProblem& fwd, const float* d_out, const 
   f.ckpt_every_chunks = 1;
   f.n_ckpt = n_ckpt;
   f.scan_segs = 0;
+  // and every token's u where the forward can write it (then the token
+  // states are rebuilt without column sums)
+  f.u_out = chunk_fwd_writes_u(B, H) ? ufwd : nullptr;
   cudaError_t e = launch_chunk_fwd(f, fwd_ws, stream);
   if (e != cudaSuccess) return e;
   BwdParams bp{static_cast<const __nv_bfloat16*>(fwd.q), static_cast<const __nv_bfloat16*>(fwd.k),
                static_cast<const __nv_bfloat16*>(fwd.v), static_cast<const __nv_bfloat16*>(fwd.log_alpha),
                static_cast<const __nv_bfloat16*>(fwd.beta), fwd.initial_state, ckpt, d_out, d_final,
-               dq, dk, dv, dla, dbeta, ds0, scratch, T, H, n_ckpt, fwd.scale};
+               dq, dk, dv, dla, dbeta, ds0, scratch, f.u_out, T, H, n_ckpt, fwd.scale};
   // dq, dk, dlog_alpha and dbeta are summed over the column blocks
   const size_t tok_bytes = (size_t)B * T * H * d * sizeof(float);
   for (float* x : {dq, dk, dla}) {

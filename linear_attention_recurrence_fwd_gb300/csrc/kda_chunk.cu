@@ -448,6 +448,9 @@ struct FusedRing {
   int* consumed;  // chain c's at consumed + c * kFlagLine
   int* counter;
   int R, ready_stride;
+  // or null: every token's u = beta (v - S'^T k), fp32, [B * T][H][d] like
+  // the output (the backward rebuilds its token states from them)
+  float* u_out;
 };
 
 // Orders this thread's global accesses between the generic proxy (the flags)
@@ -1777,6 +1780,13 @@ __device__ __forceinline__ void fused_state_body(const CUtensorMap& tm_v, const 
         }
 #pragma unroll
         for (int r0 = 0; r0 < 32; r0 += 8) st8h(layout_addr(UT, v, 32 * half + r0), u + r0);
+        if (ring.u_out && v < DIN) {  // this thread's value channel of 32 tokens
+          const int t0 = CH * (jb + j) + 32 * half;
+          float* uo = ring.u_out + ((size_t)(tok0 + t0) * H + h) * DIN + v;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (t0 + i < len) uo[(size_t)i * H * DIN] = u[i];
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
@@ -2166,16 +2176,18 @@ cudaError_t launch_stages(const ChunkProblem& pr, const CUtensorMap& tq, const C
   // per-round host copies, not the ablation, with the workspace's counters,
   // where it is the faster schedule (use_fused).  Its ring of records stays
   // in L2.
-  if (use_fused(!pr.cu_seqlens && segs == 1 && !pr.hooks && !pr.diag_per_pair && allow_overlap &&
-                    carry && grid_done,
-                pr.n_seq * pr.H, nc_max, sms)) {
+  const bool fused_ok = !pr.cu_seqlens && segs == 1 && !pr.hooks && !pr.diag_per_pair &&
+                        allow_overlap && carry && grid_done;
+  // u wanted (the backward's forward): only the fused launch writes it
+  if (pr.u_out && !(fused_ok && 2 * pr.n_seq * pr.H <= sms)) return cudaErrorNotSupported;
+  if (pr.u_out || use_fused(fused_ok, pr.n_seq * pr.H, nc_max, sms)) {
     const int chains = pr.n_seq * pr.H, R = std::min(kFusedRing, nc_max);
     // flags in the carry (not used by this path): the counter's line, a line
     // per chain for consumed, then each chain's ready slots on lines of their own
     const int ready_stride = (R + kFlagLine - 1) / kFlagLine * kFlagLine;
     int* flags = reinterpret_cast<int*>(carry);
     const FusedRing fr{flags + (size_t)(1 + chains) * kFlagLine, flags + kFlagLine, flags, R,
-                       ready_stride};
+                       ready_stride, pr.u_out};
     const size_t flag_ints = (size_t)(1 + chains) * kFlagLine + (size_t)chains * ready_stride;
     e = cudaMemsetAsync(flags, 0, flag_ints * sizeof(int), stream);
     if (e != cudaSuccess) return e;
@@ -2281,6 +2293,11 @@ int scan_segments(int B, int T, int H, int sms, int forced) {
   if (segs <= 1) return 1;
   const int per = (nc + segs - 1) / segs;  // chunks per segment
   return (nc + per - 1) / per;
+}
+
+bool chunk_fwd_writes_u(int n_seq, int H) {
+  int sms = 0;
+  return device_sms(&sms) == cudaSuccess && 2 * n_seq * H <= sms;
 }
 
 int chunk_fwd_launches(bool packed, int n_seq, int max_len, int H) {

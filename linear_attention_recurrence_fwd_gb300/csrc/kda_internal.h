@@ -57,6 +57,11 @@ struct ChunkProblem {
   int scan_segs;
   // per-round callbacks (fixed lengths without a scan only), or null
   RoundHooks* hooks = nullptr;
+  // or null: every token's u = beta (v - S'^T k), fp32, laid out like an fp32
+  // output.  Only the fused launch writes it (fixed lengths, no scan, at most
+  // half the SMs in chains: chunk_fwd_writes_u); otherwise the call returns
+  // cudaErrorNotSupported before any launch.
+  float* u_out = nullptr;
 };
 
 // Device workspace the chunked prefill needs: per-(chunk, head) records
@@ -64,6 +69,9 @@ struct ChunkProblem {
 size_t chunk_workspace_bytes(bool packed, int n_seq, long long T_or_total, int H);
 // The same for B fixed-length sequences cut into segs segments (a scan).
 size_t chunk_scan_workspace_bytes(int B, long long T, int H, int segs);
+// Whether a fixed-length forward of n_seq x H chains without a scan can
+// write u (ChunkProblem::u_out) on the current device.
+bool chunk_fwd_writes_u(int n_seq, int H);
 
 cudaError_t launch_chunk_fwd(const ChunkProblem& p, void* workspace, cudaStream_t stream);
 

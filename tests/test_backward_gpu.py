@@ -5,8 +5,10 @@ Every gradient (q, k, v, log_alpha, beta and the initial state) is compared
 element by element with the bar of tests/parity.py, each against its own
 RMS: several chunks and a ragged tail, a single partial chunk, d = 64 with
 two sequences, no initial state and no final-state gradient, slow decay (the
-gradient carries across every chunk), scale != 1, the empty sequence, and
-the 8k x 32-head problem the bench times (three heads against the oracle).
+gradient carries across every chunk), scale != 1, tokens with beta = 0 (their
+w comes from a column sum, the others' from the forward's u), the empty
+sequence, 80 chains (no u from the forward), and the 8k x 32-head problem
+the bench times (three heads against the oracle).
 """
 import numpy as np
 import pytest
@@ -28,10 +30,13 @@ def _built(cuda_device):
     build.build()
 
 
-def _case(B, T, H, d, seed, with_s0=True, with_dfin=True, slow=False, scale=1.0):
+def _case(B, T, H, d, seed, with_s0=True, with_dfin=True, slow=False, scale=1.0,
+          zero_beta=False):
     x = gen.make_inputs(B, T, H, d, d, seed, init_std=0.02)
     if slow:  # log-decay -0.05 sigmoid(N(0,1)): the gradient carries across every chunk
         x["log_alpha"] = (x["log_alpha"].float() * 0.01).to(torch.bfloat16)
+    if zero_beta:  # every 7th token writes nothing (its dbeta still needs its w)
+        x["beta"][:, ::7] = 0
     r = np.random.default_rng(seed + 1000)
     d_out = torch.from_numpy(r.standard_normal((B, T, H, d)).astype(np.float32))
     d_fin = torch.from_numpy((0.1 * r.standard_normal((B, H, d, d))).astype(np.float32))
@@ -68,6 +73,16 @@ def test_backward_without_initial_state_or_final_gradient():
 
 def test_backward_slow_decay_and_scale():
     _case(1, 320, 2, 128, seed=65, slow=True, scale=0.125)
+
+
+def test_backward_tokens_with_zero_beta():
+    _case(2, 200, 2, 128, seed=68, zero_beta=True)
+
+
+def test_backward_many_chains_without_the_forward_u():
+    """80 (sequence, head) chains: more than half the SMs, so the forward
+    cannot leave u and every token's w takes the column sum."""
+    _case(1, 130, 80, 128, seed=69)
 
 
 def test_backward_empty_sequence_passes_the_final_gradient_through():
