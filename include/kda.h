@@ -242,11 +242,14 @@ KDA_API size_t kda_chunk_fwd_host_workspace_size(int B, int T, int H, int d_k, i
  *   workspace        : kda_chunk_bwd_workspace_size(B, T, H, d_k, d_v) bytes,
  *                      16-byte aligned, owned by the caller; it holds the
  *                      forward's records, the state at every 64-token
- *                      boundary and 4 MiB (d = 128) of scratch per sequence
+ *                      boundary, every token's u (fp32, the size of an fp32
+ *                      output) and 1 MiB (d = 128) of scratch per sequence
  *                      and head.
  * Every gradient buffer is written in full.  The call runs the forward again
- * (its outputs are not written) and then one CTA per (sequence, head) over
- * the tokens in reverse, so its time grows with T per sequence and head.
+ * (its outputs are not written; where B * H is at most half the SMs it takes
+ * the fused launch, which also leaves every token's u) and then CTAs per
+ * (sequence, head, 8 value columns) over the tokens in reverse, so its time
+ * grows with T per sequence and head.
  * Errors are those of kda_chunk_fwd; a NULL gradient buffer other than
  * d_initial_state is KDA_ERR_INVALID_ARG.
  */
