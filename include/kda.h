@@ -74,7 +74,7 @@ extern "C" {
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad cu_seqlens on host */
-    KDA_ERR_UNSUPPORTED = 2, /* head dim or dtype this build does not implement   */
+    KDA_ERR_UNSUPPORTED = 2, /* head dim or dtype the library does not implement */
     KDA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned                  */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
     KDA_ERR_DECAY_BOUND = 5, /* device found log_alpha outside [-5, 0]            */
