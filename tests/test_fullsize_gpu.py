@@ -1,9 +1,11 @@
 """The named workloads against the fp64 oracle at full size, every head.
 
 * prefill_64k: B=1, T=65536, H=32, d=128, random fp32 initial state (the
-  benchmark's headline problem, same seed, same launch configuration);
+  benchmark's headline problem, same seed, same launch configuration; the
+  fused launch forced on it gives the same bits);
 * varlen_64k: four packed sequences summing to 65536 tokens, H=32;
-* long_1m: B=1, T=1,048,576, H=16, decay concentrated near the bound;
+* long_1m: B=1, T=1,048,576, H=16, decay concentrated near the bound, through
+  the segment scan kda_chunk_fwd picks and again in one fused launch without it;
 * decode: 256 sequences x 32 heads from the 64-set input pool, 128 chained
   in-place steps (step s uses set s mod 64), every step's output compared.
 
@@ -36,7 +38,7 @@ def _status_ok():
     assert st == 0, binding.kda_status_string(st)
 
 
-def test_prefill_64k_all_heads_against_oracle():
+def test_prefill_64k_all_heads_against_oracle(monkeypatch):
     w = gen.WORKLOADS["prefill_64k"]
     dev = torch.device("cuda:0")
     x = gen.workload_inputs(w, device=dev)
@@ -44,6 +46,16 @@ def test_prefill_64k_all_heads_against_oracle():
                                      out_dtype=torch.float32)
     torch.cuda.synchronize()
     _status_ok()
+    # the same call on the fused launch (which this shape does not take by
+    # itself): the same arithmetic, bit for bit
+    monkeypatch.setenv("KDA_SCHEDULE", "fused")
+    out2, fin2 = binding.kda_chunk_fwd(*[x[k] for k in KEYS], x["initial_state"],
+                                       out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    monkeypatch.delenv("KDA_SCHEDULE")
+    _status_ok()
+    assert torch.equal(out, out2) and torch.equal(fin, fin2)
+    del out2, fin2
     host = {k: x[k].cpu() for k in KEYS}
     s0 = x["initial_state"].cpu()
     o, s = out.cpu(), fin.cpu()
@@ -89,6 +101,14 @@ def test_long_1m_all_heads_against_oracle():
     torch.cuda.synchronize()
     _status_ok()
     o, s = out.cpu(), fin.cpu()
+    del out, fin
+    # without the scan: one fused launch, 16 chains whose rings of 16
+    # records wrap a thousand times
+    out, fin = binding.kda_chunk_fwd_segments(*[x[k] for k in KEYS], None, n_segments=1,
+                                              out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _status_ok()
+    o1, s1 = out.cpu(), fin.cpu()
     host = {k: x[k].cpu() for k in KEYS}
     del x, out, fin
     torch.cuda.empty_cache()
@@ -97,6 +117,8 @@ def test_long_1m_all_heads_against_oracle():
         ro, rs = orc.kda_recurrence(*[host[k][:, :, hs] for k in KEYS], None)
         assert_output_close(o[:, :, hs], ro, what=f"long_1m heads {h0}-{h0 + 1}")
         assert_state_close(s[:, hs], rs, what=f"long_1m heads {h0}-{h0 + 1} state")
+        assert_output_close(o1[:, :, hs], ro, what=f"long_1m fused heads {h0}-{h0 + 1}")
+        assert_state_close(s1[:, hs], rs, what=f"long_1m fused heads {h0}-{h0 + 1} state")
         del ro, rs
 
 
