@@ -247,8 +247,8 @@ KDA_API size_t kda_chunk_fwd_host_workspace_size(int B, int T, int H, int d_k, i
  *                      and head.
  * Every gradient buffer is written in full.  The call runs the forward again
  * (its outputs are not written; where B * H is at most half the SMs it takes
- * the fused launch, which also leaves every token's u) and then CTAs per
- * (sequence, head, 8 value columns) over the tokens in reverse, so its time
+ * the fused launch, which also leaves every token's u) and then one warp per
+ * (sequence, head, 4 value columns) over the tokens in reverse, so its time
  * grows with T per sequence and head.
  * Errors are those of kda_chunk_fwd; a NULL gradient buffer other than
  * d_initial_state is KDA_ERR_INVALID_ARG.

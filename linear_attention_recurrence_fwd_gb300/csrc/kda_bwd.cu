@@ -15,19 +15,18 @@
 //
 // Layout of the work: the forward (the chunked tensor-core path) saves the
 // state at every chunk boundary and, where it can (the fused launch), every
-// token's u; one CTA per (sequence, head, block of 8 value columns) then
+// token's u; one warp per (sequence, head, block of 4 value columns) then
 // walks the chunks from last to first.  For each chunk it rebuilds the token
 // states in fp32 from the saved chunk-start state: with u given that is a
 // local step per token (S'_t = Diag(alpha_t) S_{t-1}, S_t = S'_t + k_t u_t^T,
 // w_t = u_t / beta_t), and only without it, or for a token with beta = 0,
 // does w take a column sum.  It keeps the state before every 4th token (in a
-// per-CTA scratch in global memory) and, in the reverse recurrence, rebuilds
-// each group of 4 token states in registers from it.  Thread c holds row c of
-// G for the block's columns in registers: dot products along a row stay in
-// the thread, sums down a column (du, and w without u) take a warp
-// reduce-scatter and one pass over shared memory.  This is CUDA-core work,
-// serial in tokens per (sequence, head): an exact token-level formulation,
-// not a tensor-core one.
+// per-warp scratch in global memory) and, in the reverse recurrence, rebuilds
+// each group of 4 token states in registers from it.  Lane l holds d_k / 32
+// consecutive rows of G for the warp's columns in registers: dot products
+// along a row stay in the lane, sums down a column (du, and w without u) are
+// a butterfly over the warp.  This is CUDA-core work, serial in tokens per
+// (sequence, head): an exact token-level formulation, not a tensor-core one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -48,72 +47,95 @@ struct BwdParams {
   const float* dout;  // [B][T][H][d]
   const float* dfin;  // [B][H][d][d] or null (zeros)
   float *dq, *dk, *dv, *dla, *dbeta, *ds0;
-  float* scratch;      // [B * H][64 / SUB][d][d]
+  float* scratch;      // [B * H][d / CW][64 / SUB][d][CW]: per warp, the state before each sub-block
   const float* u_fwd;  // [B][T][H][d]: every token's u from the forward (HAVE_U), or null
   int T, H, n_ckpt;
   float scale;
 };
 
-// One CTA per (sequence, head, block of CB value columns): the columns of G
-// evolve independently (each step scales rows and adds rank-one terms), so
-// only the gradients summed along a row (dq, dk, dlog_alpha, dbeta) combine
-// the blocks, by atomic adds into zeroed buffers.  Thread c owns key row c
-// and the block's CB columns.
-constexpr int CB = 8;
+// Work split.  The columns of G evolve independently (each step scales rows
+// and adds rank-one terms), so a warp owns a block of CW value columns for
+// all d_k key rows, lane l the RL = d_k / 32 consecutive rows RL l, ...:
+// a sum down a column (du, and w without u) is then a butterfly over the
+// warp's lanes with no barrier.  Only the gradients summed along a row (dq,
+// dk, dlog_alpha, dbeta) join the column blocks, by atomic adds into zeroed
+// buffers.  A CTA of WPC warps (WPC column blocks of one (sequence, head))
+// stages each chunk's token rows once for all its warps; the warps meet only
+// at the chunk boundaries.
+constexpr int CW = 4;   // value columns per warp (one float4 per key row)
+constexpr int WPC = 4;  // warps per CTA
 // Tokens per sub-block of the reverse pass: the state before each sub-block
-// is saved (in the per-CTA scratch), and the sub-block's token states are
+// is saved (in the per-warp scratch), and the sub-block's token states are
 // rebuilt in registers when the reverse pass reaches it.
 constexpr int SUB = 4;
 
 template <int DIN>
 struct BwdShape {
-  static constexpr int THREADS = DIN;  // one thread per key row
-  static constexpr int WARPS = THREADS / 32;
-  static constexpr int BLOCKS = DIN / CB;
-  // shared memory: q, k, log alpha (bf16, every channel), the block's v
-  // (bf16), do, u, w (fp32), the column-sum partials, one vector, beta
+  static constexpr int RL = DIN / 32;  // key rows per lane
+  static constexpr int THREADS = 32 * WPC;
+  static constexpr int COLS = CW * WPC;    // value columns per CTA
+  static constexpr int CTAS = DIN / COLS;  // CTAs per (sequence, head)
+  // shared memory: q, k, log alpha (bf16, every channel), the CTA's v
+  // columns (bf16), its do, u and w columns (fp32), beta
   static constexpr size_t OFF_Q = 0;
   static constexpr size_t OFF_K = OFF_Q + BW_CH * DIN * 2;
   static constexpr size_t OFF_LA = OFF_K + BW_CH * DIN * 2;
   static constexpr size_t OFF_V = OFF_LA + BW_CH * DIN * 2;
-  static constexpr size_t OFF_DO = OFF_V + BW_CH * CB * 2;
-  static constexpr size_t OFF_U = OFF_DO + BW_CH * CB * 4;
-  static constexpr size_t OFF_W = OFF_U + BW_CH * CB * 4;
-  static constexpr size_t OFF_RED = OFF_W + BW_CH * CB * 4;
-  static constexpr size_t OFF_VEC = OFF_RED + WARPS * CB * 4;
-  static constexpr size_t OFF_BETA = OFF_VEC + CB * 4;
+  static constexpr size_t OFF_DO = OFF_V + BW_CH * COLS * 2;
+  static constexpr size_t OFF_U = OFF_DO + BW_CH * COLS * 4;
+  static constexpr size_t OFF_W = OFF_U + BW_CH * COLS * 4;
+  static constexpr size_t OFF_BETA = OFF_W + BW_CH * COLS * 4;
   static constexpr size_t SMEM = OFF_BETA + BW_CH * 4;
 };
+static_assert(CW == 4, "a lane's share of a key row is one float4");
 
 __device__ __forceinline__ float bfv(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
 }
 
-// Sum of x over the warp's 32 rows for each of the CB columns: a
-// reduce-scatter over lane bits 4, 3, .. (one halving per bit, log2 CB
-// steps) leaves the lanes that differ only in the remaining low bits with
-// partial sums of one column, which a few exchanges add; the first of them
-// writes red[warp][column].  The caller synchronises and adds the warps.
-static_assert(CB == 8 || CB == 16 || CB == 32, "column blocks of 8, 16 or 32");
-constexpr int LOG_CB = CB == 8 ? 3 : CB == 16 ? 4 : 5;
-__device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int warp, int lane) {
-#pragma unroll
-  for (int step = 0; step < LOG_CB; ++step) {
-    const int bit = 16 >> step;         // lane bit 4, 3, ...
-    const int half = CB >> (step + 1);  // values kept after this step
-    const bool up = (lane & bit) != 0;  // keep the upper half of the current range
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = up ? x[i] : x[i + half];
-      float keep = up ? x[i + half] : x[i];
-      keep += __shfl_xor_sync(0xffffffffu, send, bit);
-      x[i] = keep;
-    }
+// The lane's RL consecutive bf16 entries of a staged token row, as floats.
+template <int RL>
+__device__ __forceinline__ void ld_rows(const __nv_bfloat16* src, float (&x)[RL]) {
+  if constexpr (RL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+    x[0] = __uint_as_float(u << 16);
+    x[1] = __uint_as_float(u & 0xffff0000u);
   }
-  constexpr int LOW = 5 - LOG_CB;  // lane bits left: the same column on 2^LOW lanes
+}
+
+// Column sums over the warp's lanes, left on every lane: a reduce-scatter
+// over lane bits 4 and 3 (each lane then holds one column's partial), a sum
+// over bits 2, 1, 0, and one broadcast per column, so that every lane ends
+// with the same bits.
+__device__ __forceinline__ void warp_sum(float (&y)[CW], int lane) {
+  const bool up = (lane & 16) != 0, up8 = (lane & 8) != 0;
+  float k0 = up ? y[2] : y[0], k1 = up ? y[3] : y[1];
+  k0 += __shfl_xor_sync(0xffffffffu, up ? y[0] : y[2], 16);
+  k1 += __shfl_xor_sync(0xffffffffu, up ? y[1] : y[3], 16);
+  float k = up8 ? k1 : k0;  // column 2 (lane bit 4) + (lane bit 3)
+  k += __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
 #pragma unroll
-  for (int o = 1; o < (1 << LOW); o <<= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
-  if ((lane & ((1 << LOW) - 1)) == 0) red[warp * CB + (lane >> LOW)] = x[0];
+  for (int j = 0; j < CW; ++j) y[j] = __shfl_sync(0xffffffffu, k, (j >> 1) * 16 + (j & 1) * 8);
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Row sums of one token for the lane's RL key rows, added into a gradient.
+template <int RL>
+__device__ __forceinline__ void add_rows(float* dst, const float (&x)[RL]) {
+  if constexpr (RL == 4)
+    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(x[0], x[1], x[2], x[3]));
+  else
+    atomicAdd(reinterpret_cast<float2*>(dst), make_float2(x[0], x[1]));
 }
 
 // HAVE_U: the forward left every token's u, so the chunk's token states
@@ -122,6 +144,7 @@ __device__ __forceinline__ void column_partials(float (&x)[CB], float* red, int 
 template <int DIN, bool HAVE_U>
 __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdParams p) {
   using S = BwdShape<DIN>;
+  constexpr int RL = S::RL, COLS = S::COLS;
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* sq = reinterpret_cast<__nv_bfloat16*>(smem + S::OFF_Q);
   __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(smem + S::OFF_K);
@@ -130,40 +153,59 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
   float* sdo = reinterpret_cast<float*>(smem + S::OFF_DO);
   float* su = reinterpret_cast<float*>(smem + S::OFF_U);
   float* sw = reinterpret_cast<float*>(smem + S::OFF_W);
-  float* red = reinterpret_cast<float*>(smem + S::OFF_RED);
-  float* svec = reinterpret_cast<float*>(smem + S::OFF_VEC);
   float* sbeta = reinterpret_cast<float*>(smem + S::OFF_BETA);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = tid;  // key row
-  const int h = blockIdx.x, n = blockIdx.y, blk = blockIdx.z, vb = CB * blk;  // first column
+  const int h = blockIdx.x, n = blockIdx.y;
+  const int cb = COLS * blockIdx.z;  // the CTA's first value column
+  const int wc = CW * warp;          // the warp's first column within the CTA's
+  const int vb = cb + wc;            // the warp's first value column
+  const int r0 = RL * lane;          // the lane's first key row
   const int H = p.H, T = p.T;
   const size_t dd = (size_t)DIN * DIN;
-  const size_t plane = ((size_t)n * H + h) * dd;     // this (sequence, head) in [B][H][d][d]
-  const size_t row = plane + (size_t)c * DIN + vb;  // element (c, vb)
-  // per-thread scratch of one chunk: the state before each sub-block, this
-  // thread's CB values
-  float* scratch = p.scratch + (((size_t)n * H + h) * S::BLOCKS + blk) * (BW_CH / SUB) * DIN * CB +
-                   (size_t)tid * CB;
+  const size_t plane = ((size_t)n * H + h) * dd;  // this (sequence, head) in [B][H][d][d]
+  // the warp's scratch of one chunk: the state before each sub-block, laid
+  // out [sub-block][lane][RL rows][CW columns]
+  float* scratch = p.scratch + (((size_t)n * H + h) * (DIN / CW) + vb / CW) * (BW_CH / SUB) * DIN * CW +
+                   (size_t)lane * RL * CW;
 
-  auto load_row = [&](const float* src, float (&x)[CB]) {  // x = src[c][vb .. vb + CB)
+  // x = the lane's rows of columns vb .. vb + CW of a [d][d] plane (zeros for null)
+  auto load_state = [&](const float* src, float (&x)[RL][CW]) {
 #pragma unroll
-    for (int j = 0; j < CB; j += 4) {
-      const float4 f = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x[j] = f.x;
-      x[j + 1] = f.y;
-      x[j + 2] = f.z;
-      x[j + 3] = f.w;
+    for (int m = 0; m < RL; ++m) {
+      const float4 f = src ? ld4(src + (size_t)(r0 + m) * DIN + vb) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[m][0] = f.x;
+      x[m][1] = f.y;
+      x[m][2] = f.z;
+      x[m][3] = f.w;
     }
   };
-  float g[CB];  // G[c][vb ..]: the gradient of the state after the current token
-  load_row(p.dfin ? p.dfin + row : nullptr, g);
+  auto save_sub = [&](int sb, const float (&x)[RL][CW]) {
+    float* dst = scratch + (size_t)sb * DIN * CW;
+#pragma unroll
+    for (int m = 0; m < RL; ++m)
+      *reinterpret_cast<float4*>(dst + m * CW) = make_float4(x[m][0], x[m][1], x[m][2], x[m][3]);
+  };
+  auto load_sub = [&](int sb, float (&x)[RL][CW]) {
+    const float* src = scratch + (size_t)sb * DIN * CW;
+#pragma unroll
+    for (int m = 0; m < RL; ++m) {
+      const float4 f = ld4(src + m * CW);
+      x[m][0] = f.x;
+      x[m][1] = f.y;
+      x[m][2] = f.z;
+      x[m][3] = f.w;
+    }
+  };
+
+  float g[RL][CW];  // G for the lane's rows and the warp's columns: the gradient of the state after the current token
+  load_state(p.dfin ? p.dfin + plane : nullptr, g);
 
   const int nch = (T + BW_CH - 1) / BW_CH;
   for (int ch = nch - 1; ch >= 0; --ch) {
     const int t0 = ch * BW_CH, L = min(BW_CH, T - t0);
-    // ---- stage the chunk's token rows
-    __syncthreads();  // the previous chunk is done with shared memory
+    // ---- stage the chunk's token rows (the CTA's columns of v, do and u)
+    __syncthreads();  // every warp is done with the previous chunk
     for (int e = tid; e < BW_CH * DIN / 8; e += S::THREADS) {  // 8 bf16 (16 bytes) at a time
       const int i = e / (DIN / 8), c8 = (e % (DIN / 8)) * 8;
       uint4 zq = make_uint4(0, 0, 0, 0), zk = zq, zl = zq;
@@ -177,157 +219,205 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
       *reinterpret_cast<uint4*>(sk + i * DIN + c8) = zk;
       *reinterpret_cast<uint4*>(sla + i * DIN + c8) = zl;
     }
-    for (int e = tid; e < BW_CH * CB / 8; e += S::THREADS) {  // the block's v columns
-      const int i = e / (CB / 8), c8 = (e % (CB / 8)) * 8;
+    for (int e = tid; e < BW_CH * COLS / 8; e += S::THREADS) {
+      const int i = e / (COLS / 8), c8 = (e % (COLS / 8)) * 8;
       uint4 z = make_uint4(0, 0, 0, 0);
-      if (i < L) z = *reinterpret_cast<const uint4*>(p.v + (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c8);
-      *reinterpret_cast<uint4*>(sv + i * CB + c8) = z;
+      if (i < L) z = *reinterpret_cast<const uint4*>(p.v + (((size_t)n * T + t0 + i) * H + h) * DIN + cb + c8);
+      *reinterpret_cast<uint4*>(sv + i * COLS + c8) = z;
     }
-    for (int e = tid; e < BW_CH * CB / 4; e += S::THREADS) {  // the block's do (and u) columns
-      const int i = e / (CB / 4), c4 = (e % (CB / 4)) * 4;
-      const size_t off = (((size_t)n * T + t0 + i) * H + h) * DIN + vb + c4;
+    for (int e = tid; e < BW_CH * COLS / 4; e += S::THREADS) {
+      const int i = e / (COLS / 4), c4 = (e % (COLS / 4)) * 4;
+      const size_t off = (((size_t)n * T + t0 + i) * H + h) * DIN + cb + c4;
       float4 z = make_float4(0.f, 0.f, 0.f, 0.f), zu = z;
       if (i < L) {
-        z = *reinterpret_cast<const float4*>(p.dout + off);
-        if (HAVE_U) zu = *reinterpret_cast<const float4*>(p.u_fwd + off);
+        z = ld4(p.dout + off);
+        if (HAVE_U) zu = ld4(p.u_fwd + off);
       }
-      *reinterpret_cast<float4*>(sdo + i * CB + c4) = z;
-      if (HAVE_U) *reinterpret_cast<float4*>(su + i * CB + c4) = zu;
+      *reinterpret_cast<float4*>(sdo + i * COLS + c4) = z;
+      if (HAVE_U) *reinterpret_cast<float4*>(su + i * COLS + c4) = zu;
     }
     if (tid < BW_CH) sbeta[tid] = tid < L ? bfv(p.beta, ((size_t)n * T + t0 + tid) * H + h) : 0.f;
     __syncthreads();
 
-    // ---- forward over the chunk from its saved starting state
-    float s[CB];
+    // ---- forward over the chunk from its saved starting state (each warp alone)
     {
-      const float* src = ch == 0 ? (p.s0 ? p.s0 + plane : nullptr)
-                                 : p.ckpt + (((size_t)n * p.n_ckpt + (ch - 1)) * H + h) * dd;
-      load_row(src ? src + (size_t)c * DIN + vb : nullptr, s);
-    }
-    for (int i = 0; i < L; ++i) {
-      const float a = __expf(__bfloat162float(sla[i * DIN + c]));
-      const float kc = __bfloat162float(sk[i * DIN + c]);
-      if ((i & (SUB - 1)) == 0) {  // S_{t-1}: the state before this sub-block
-        float* dst = scratch + (size_t)(i / SUB) * DIN * CB;
+      float s[RL][CW];
+      load_state(ch == 0 ? (p.s0 ? p.s0 + plane : nullptr)
+                         : p.ckpt + (((size_t)n * p.n_ckpt + (ch - 1)) * H + h) * dd,
+                 s);
+      for (int i = 0; i < L; ++i) {
+        float a[RL], kc[RL];
+        ld_rows<RL>(sla + i * DIN + r0, a);
+        ld_rows<RL>(sk + i * DIN + r0, kc);
+        if ((i & (SUB - 1)) == 0) save_sub(i / SUB, s);  // S_{t-1}: the state before this sub-block
 #pragma unroll
-        for (int j = 0; j < CB; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-      }
-      float x[CB];
+        for (int m = 0; m < RL; ++m) {
+          a[m] = __expf(a[m]);
 #pragma unroll
-      for (int j = 0; j < CB; ++j) {
-        s[j] *= a;  // S'_t
-        x[j] = s[j] * kc;
-      }
-      const float b = sbeta[i];
-      if (!HAVE_U || b == 0.f) {  // (with u given: the same for every thread)
-        column_partials(x, red, warp, lane);
-        __syncthreads();
-        if (tid < CB) {  // w = v - S'^T k, u = beta w
-          float acc = 0.f;
-#pragma unroll
-          for (int wp = 0; wp < S::WARPS; ++wp) acc += red[wp * CB + tid];
-          const float w = __bfloat162float(sv[i * CB + tid]) - acc;
-          sw[i * CB + tid] = w;
-          su[i * CB + tid] = b * w;
+          for (int j = 0; j < CW; ++j) s[m][j] *= a[m];  // S'_t
         }
-        __syncthreads();
-      }
+        float u[CW];
+        const float b = sbeta[i];
+        if (!HAVE_U || b == 0.f) {  // (the same on every lane) w = v - S'^T k, u = beta w
+          float y[CW];
 #pragma unroll
-      for (int j = 0; j < CB; ++j) s[j] += kc * su[i * CB + j];  // S_t
-    }
-    if (HAVE_U) {  // w = u / beta where beta != 0
-      for (int e = tid; e < L * CB; e += S::THREADS) {
-        const float b = sbeta[e / CB];
-        if (b != 0.f) sw[e] = su[e] / b;
+          for (int j = 0; j < CW; ++j) {
+            y[j] = 0.f;
+#pragma unroll
+            for (int m = 0; m < RL; ++m) y[j] += s[m][j] * kc[m];
+          }
+          warp_sum(y, lane);
+          float w[CW];
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            w[j] = __bfloat162float(sv[i * COLS + wc + j]) - y[j];
+            u[j] = b * w[j];
+          }
+          if (lane == 0) {
+            *reinterpret_cast<float4*>(sw + i * COLS + wc) = make_float4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<float4*>(su + i * COLS + wc) = make_float4(u[0], u[1], u[2], u[3]);
+          }
+        } else {
+          const float4 f = ld4(su + i * COLS + wc);
+          u[0] = f.x;
+          u[1] = f.y;
+          u[2] = f.z;
+          u[3] = f.w;
+        }
+#pragma unroll
+        for (int m = 0; m < RL; ++m) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) s[m][j] += kc[m] * u[j];  // S_t
+        }
       }
-      __syncthreads();
     }
+    if (HAVE_U) {  // w = u / beta where beta != 0 (the warp's columns)
+      for (int e = lane; e < L * CW; e += 32) {
+        const int i = e / CW, j = e % CW;
+        const float b = sbeta[i];
+        if (b != 0.f) sw[i * COLS + wc + j] = su[i * COLS + wc + j] / b;
+      }
+    }
+    __syncwarp();
 
     // ---- the reverse recurrence over the chunk's tokens, SUB at a time: the
     // sub-block's S'_t are rebuilt in registers from the state saved before
     // it (a local step per token: u is known), whose load is issued one
     // sub-block ahead.
     const int nsub = (L + SUB - 1) / SUB;
-    float nxt[CB];
-    if (nsub > 0) load_row(scratch + (size_t)(nsub - 1) * DIN * CB, nxt);
+    float nxt[RL][CW];
+    if (nsub > 0) load_sub(nsub - 1, nxt);
     for (int sbk = nsub - 1; sbk >= 0; --sbk) {
-      float spq[SUB][CB];
+      float spq[SUB][RL][CW];
       {
-        float st[CB];
+        float st[RL][CW];
 #pragma unroll
-        for (int j = 0; j < CB; ++j) st[j] = nxt[j];
-        if (sbk > 0) load_row(scratch + (size_t)(sbk - 1) * DIN * CB, nxt);
+        for (int m = 0; m < RL; ++m) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) st[m][j] = nxt[m][j];
+        }
+        if (sbk > 0) load_sub(sbk - 1, nxt);
 #pragma unroll
         for (int q = 0; q < SUB; ++q) {
           const int i = SUB * sbk + q;
-          const float a = i < L ? __expf(__bfloat162float(sla[i * DIN + c])) : 1.f;
-          const float kc = i < L ? __bfloat162float(sk[i * DIN + c]) : 0.f;
+          float a[RL], kc[RL], u[CW];
+          if (i < L) {
+            ld_rows<RL>(sla + i * DIN + r0, a);
+            ld_rows<RL>(sk + i * DIN + r0, kc);
+            const float4 f = ld4(su + i * COLS + wc);
+            u[0] = f.x;
+            u[1] = f.y;
+            u[2] = f.z;
+            u[3] = f.w;
 #pragma unroll
-          for (int j = 0; j < CB; ++j) {
-            st[j] *= a;
-            spq[q][j] = st[j];
-            st[j] += kc * su[(i < L ? i : 0) * CB + j];
+            for (int m = 0; m < RL; ++m) a[m] = __expf(a[m]);
+          } else {
+#pragma unroll
+            for (int m = 0; m < RL; ++m) {
+              a[m] = 1.f;
+              kc[m] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < CW; ++j) u[j] = 0.f;
+          }
+#pragma unroll
+          for (int m = 0; m < RL; ++m) {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+              st[m][j] *= a[m];
+              spq[q][m][j] = st[m][j];
+              st[m][j] += kc[m] * u[j];
+            }
           }
         }
       }
 #pragma unroll
-    for (int q = SUB - 1; q >= 0; --q) {
-      const int i = SUB * sbk + q;
-      if (i >= L) continue;  // (the same for every thread)
-      const size_t tok = ((size_t)n * T + t0 + i) * H + h;
-      const float* sp = spq[q];
-      const float qc = __bfloat162float(sq[i * DIN + c]);
-      const float kc = __bfloat162float(sk[i * DIN + c]);
-      const float a = __expf(__bfloat162float(sla[i * DIN + c]));
-      const float b = sbeta[i];
-      const float* dov = sdo + i * CB;
-      const float* uv = su + i * CB;
-      // G += scale q do^T, then du = G^T k
-      float x[CB];
+      for (int q = SUB - 1; q >= 0; --q) {
+        const int i = SUB * sbk + q;
+        if (i >= L) continue;  // (the same on every lane)
+        const size_t tok = ((size_t)n * T + t0 + i) * H + h;
+        float qc[RL], kc[RL], a[RL];
+        ld_rows<RL>(sq + i * DIN + r0, qc);
+        ld_rows<RL>(sk + i * DIN + r0, kc);
+        ld_rows<RL>(sla + i * DIN + r0, a);
+        const float b = sbeta[i];
+        const float4 d4 = ld4(sdo + i * COLS + wc), u4 = ld4(su + i * COLS + wc),
+                     w4 = ld4(sw + i * COLS + wc);
+        const float dov[CW] = {d4.x, d4.y, d4.z, d4.w}, uv[CW] = {u4.x, u4.y, u4.z, u4.w};
+        // G += scale q do^T, then du = G^T k
+        float du[CW];
 #pragma unroll
-      for (int j = 0; j < CB; ++j) {
-        g[j] += p.scale * qc * dov[j];
-        x[j] = g[j] * kc;
-      }
-      column_partials(x, red, warp, lane);
-      __syncthreads();
-      if (warp == 0) {  // du, dv = beta du, and this block's share of dbeta = du . w
-        float du = 0.f, xb = 0.f;
-        if (lane < CB) {
+        for (int j = 0; j < CW; ++j) du[j] = 0.f;
 #pragma unroll
-          for (int wp = 0; wp < S::WARPS; ++wp) du += red[wp * CB + lane];
-          svec[lane] = du;
-          p.dv[tok * DIN + vb + lane] = b * du;
-          xb = du * sw[i * CB + lane];
+        for (int m = 0; m < RL; ++m) {
+          const float sq_m = p.scale * qc[m];
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            g[m][j] += sq_m * dov[j];
+            du[j] += g[m][j] * kc[m];
+          }
         }
+        warp_sum(du, lane);
+        if (lane == 0) {  // dv = beta du, and this block's share of dbeta = du . w
+          *reinterpret_cast<float4*>(p.dv + tok * DIN + vb) =
+              make_float4(b * du[0], b * du[1], b * du[2], b * du[3]);
+          atomicAdd(p.dbeta + tok, du[0] * w4.x + du[1] * w4.y + du[2] * w4.z + du[3] * w4.w);
+        }
+        // dq = scale S_t do with S_t = S' + k u^T;  dk = G u - beta S' du;
+        // dS' = G - beta k du^T;  dlog_alpha = rowsum(dS' o S')  (this warp's columns)
+        float ud = 0.f;  // u . do, the same on every row
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) xb += __shfl_xor_sync(0xffffffffu, xb, o);
-        if (lane == 0) atomicAdd(p.dbeta + tok, xb);
-      }
-      __syncthreads();
-      // dq = scale S_t do with S_t = S' + k u^T;  dk = G u - beta S' du;
-      // dS' = G - beta k du^T;  dlog_alpha = rowsum(dS' o S')  (this block's columns)
-      float xq = 0.f, xk = 0.f, xa = 0.f;
+        for (int j = 0; j < CW; ++j) ud += uv[j] * dov[j];
+        float xq[RL], xk[RL], xa[RL];
 #pragma unroll
-      for (int j = 0; j < CB; ++j) {
-        const float du = svec[j], u = uv[j];
-        xq += (sp[j] + kc * u) * dov[j];
-        xk += g[j] * u - b * sp[j] * du;
-        g[j] -= b * kc * du;
-        xa += g[j] * sp[j];
-        g[j] *= a;  // the gradient of S_{t-1}
+        for (int m = 0; m < RL; ++m) {
+          const float* sp = spq[q][m];
+          const float am = __expf(a[m]), bk = b * kc[m];
+          float aq = 0.f, gu = 0.f, sd = 0.f, aa = 0.f;
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            aq += sp[j] * dov[j];
+            gu += g[m][j] * uv[j];
+            sd += sp[j] * du[j];
+            g[m][j] -= bk * du[j];
+            aa += g[m][j] * sp[j];
+            g[m][j] *= am;  // the gradient of S_{t-1}
+          }
+          xq[m] = p.scale * (aq + kc[m] * ud);
+          xk[m] = gu - b * sd;
+          xa[m] = aa;
+        }
+        add_rows<RL>(p.dq + tok * DIN + r0, xq);
+        add_rows<RL>(p.dk + tok * DIN + r0, xk);
+        add_rows<RL>(p.dla + tok * DIN + r0, xa);
       }
-      atomicAdd(p.dq + tok * DIN + c, p.scale * xq);
-      atomicAdd(p.dk + tok * DIN + c, xk);
-      atomicAdd(p.dla + tok * DIN + c, xa);
-    }
     }
   }
   if (p.ds0) {
 #pragma unroll
-    for (int j = 0; j < CB; j += 4)
-      *reinterpret_cast<float4*>(p.ds0 + row + j) = make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
+    for (int m = 0; m < RL; ++m)
+      *reinterpret_cast<float4*>(p.ds0 + plane + (size_t)(r0 + m) * DIN + vb) =
+          make_float4(g[m][0], g[m][1], g[m][2], g[m][3]);
   }
 }
 
@@ -338,7 +428,7 @@ cudaError_t launch_bwd_kernel(const BwdParams& bp, int B, int H, cudaStream_t st
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
   if (e != cudaSuccess) return e;
   kda_bwd_kernel<DIN, HAVE_U>
-      <<<dim3((unsigned)H, (unsigned)B, S::BLOCKS), S::THREADS, S::SMEM, stream>>>(bp);
+      <<<dim3((unsigned)H, (unsigned)B, S::CTAS), S::THREADS, S::SMEM, stream>>>(bp);
   return cudaGetLastError();
 }
 template <int DIN>
