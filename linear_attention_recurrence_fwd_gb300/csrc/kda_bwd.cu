@@ -62,7 +62,10 @@ struct BwdParams {
 // buffers.  A CTA of WPC warps (WPC column blocks of one (sequence, head))
 // stages each chunk's token rows once for all its warps; the warps meet only
 // at the chunk boundaries.
-constexpr int CW = 4;   // value columns per warp (one float4 per key row)
+// Measured on the 8k problem: CW = 4 with 4 warps per CTA 6.8 ms; CW = 2
+// 7.9-8.2 ms (more warps, more work per column); CW = 8 8.7-8.9 ms (fewer
+// warps, 208-254 registers).
+constexpr int CW = 4;   // value columns per warp
 constexpr int WPC = 4;  // warps per CTA
 // Tokens per sub-block of the reverse pass: the state before each sub-block
 // is saved (in the per-warp scratch), and the sub-block's token states are
@@ -75,6 +78,7 @@ struct BwdShape {
   static constexpr int THREADS = 32 * WPC;
   static constexpr int COLS = CW * WPC;    // value columns per CTA
   static constexpr int CTAS = DIN / COLS;  // CTAs per (sequence, head)
+  static_assert(COLS % 8 == 0 && DIN % COLS == 0, "whole 16-byte rows of v staged per CTA");
   // shared memory: q, k, log alpha (bf16, every channel), the CTA's v
   // columns (bf16), its do, u and w columns (fp32), beta
   static constexpr size_t OFF_Q = 0;
@@ -87,7 +91,7 @@ struct BwdShape {
   static constexpr size_t OFF_BETA = OFF_W + BW_CH * COLS * 4;
   static constexpr size_t SMEM = OFF_BETA + BW_CH * 4;
 };
-static_assert(CW == 4, "a lane's share of a key row is one float4");
+static_assert(CW == 2 || CW == 4 || CW == 8, "a lane's share of a key row is 8, 16 or 32 bytes");
 
 __device__ __forceinline__ float bfv(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
@@ -110,24 +114,85 @@ __device__ __forceinline__ void ld_rows(const __nv_bfloat16* src, float (&x)[RL]
 }
 
 // Column sums over the warp's lanes, left on every lane: a reduce-scatter
-// over lane bits 4 and 3 (each lane then holds one column's partial), a sum
-// over bits 2, 1, 0, and one broadcast per column, so that every lane ends
-// with the same bits.
+// over the top lane bits (each lane then holds one column's partial), a sum
+// over the remaining bits, and one broadcast per column, so that every lane
+// ends with the same bits.
 __device__ __forceinline__ void warp_sum(float (&y)[CW], int lane) {
-  const bool up = (lane & 16) != 0, up8 = (lane & 8) != 0;
-  float k0 = up ? y[2] : y[0], k1 = up ? y[3] : y[1];
-  k0 += __shfl_xor_sync(0xffffffffu, up ? y[0] : y[2], 16);
-  k1 += __shfl_xor_sync(0xffffffffu, up ? y[1] : y[3], 16);
-  float k = up8 ? k1 : k0;  // column 2 (lane bit 4) + (lane bit 3)
-  k += __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8);
-  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  const bool up = (lane & 16) != 0;
+  float k;
+  if constexpr (CW == 8) {
+    const bool up8 = (lane & 8) != 0, up4 = (lane & 4) != 0;
+    float k4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      k4[i] = up ? y[i + 4] : y[i];
+      k4[i] += __shfl_xor_sync(0xffffffffu, up ? y[i] : y[i + 4], 16);
+    }
+    float k2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      k2[i] = up8 ? k4[i + 2] : k4[i];
+      k2[i] += __shfl_xor_sync(0xffffffffu, up8 ? k4[i] : k4[i + 2], 8);
+    }
+    k = up4 ? k2[1] : k2[0];  // column 4 (lane bit 4) + 2 (lane bit 3) + (lane bit 2)
+    k += __shfl_xor_sync(0xffffffffu, up4 ? k2[0] : k2[1], 4);
+  } else if constexpr (CW == 4) {
+    const bool up8 = (lane & 8) != 0;
+    float k0 = up ? y[2] : y[0], k1 = up ? y[3] : y[1];
+    k0 += __shfl_xor_sync(0xffffffffu, up ? y[0] : y[2], 16);
+    k1 += __shfl_xor_sync(0xffffffffu, up ? y[1] : y[3], 16);
+    k = up8 ? k1 : k0;  // column 2 (lane bit 4) + (lane bit 3)
+    k += __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8);
+  } else {
+    k = up ? y[1] : y[0];  // column (lane bit 4)
+    k += __shfl_xor_sync(0xffffffffu, up ? y[0] : y[1], 16);
+    k += __shfl_xor_sync(0xffffffffu, k, 8);
+  }
+  if constexpr (CW != 8) k += __shfl_xor_sync(0xffffffffu, k, 4);
   k += __shfl_xor_sync(0xffffffffu, k, 2);
   k += __shfl_xor_sync(0xffffffffu, k, 1);
 #pragma unroll
-  for (int j = 0; j < CW; ++j) y[j] = __shfl_sync(0xffffffffu, k, (j >> 1) * 16 + (j & 1) * 8);
+  for (int j = 0; j < CW; ++j)
+    y[j] = __shfl_sync(0xffffffffu, k,
+                       CW == 8   ? (j >> 2) * 16 + ((j >> 1) & 1) * 8 + (j & 1) * 4
+                       : CW == 4 ? (j >> 1) * 16 + (j & 1) * 8
+                                 : j * 16);
 }
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+// CW consecutive floats (one vector): x = p[0 .. CW), p[0 .. CW) = x
+__device__ __forceinline__ void ldw(const float* p, float (&x)[CW]) {
+  if constexpr (CW == 8) {
+    const float4 f = ld4(p), h = ld4(p + 4);
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+    x[4] = h.x;
+    x[5] = h.y;
+    x[6] = h.z;
+    x[7] = h.w;
+  } else if constexpr (CW == 4) {
+    const float4 f = ld4(p);
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  } else {
+    const float2 f = *reinterpret_cast<const float2*>(p);
+    x[0] = f.x;
+    x[1] = f.y;
+  }
+}
+__device__ __forceinline__ void stw(float* p, const float (&x)[CW]) {
+  if constexpr (CW == 8) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  } else if constexpr (CW == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+}
 
 // Row sums of one token for the lane's RL key rows, added into a gradient.
 template <int RL>
@@ -173,28 +238,25 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
   auto load_state = [&](const float* src, float (&x)[RL][CW]) {
 #pragma unroll
     for (int m = 0; m < RL; ++m) {
-      const float4 f = src ? ld4(src + (size_t)(r0 + m) * DIN + vb) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x[m][0] = f.x;
-      x[m][1] = f.y;
-      x[m][2] = f.z;
-      x[m][3] = f.w;
+      if (src) {
+        ldw(src + (size_t)(r0 + m) * DIN + vb, x[m]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < CW; ++j) x[m][j] = 0.f;
+      }
     }
   };
   auto save_sub = [&](int sb, const float (&x)[RL][CW]) {
     float* dst = scratch + (size_t)sb * DIN * CW;
 #pragma unroll
     for (int m = 0; m < RL; ++m)
-      *reinterpret_cast<float4*>(dst + m * CW) = make_float4(x[m][0], x[m][1], x[m][2], x[m][3]);
+      stw(dst + m * CW, x[m]);
   };
   auto load_sub = [&](int sb, float (&x)[RL][CW]) {
     const float* src = scratch + (size_t)sb * DIN * CW;
 #pragma unroll
     for (int m = 0; m < RL; ++m) {
-      const float4 f = ld4(src + m * CW);
-      x[m][0] = f.x;
-      x[m][1] = f.y;
-      x[m][2] = f.z;
-      x[m][3] = f.w;
+      ldw(src + m * CW, x[m]);
     }
   };
 
@@ -274,15 +336,11 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
             u[j] = b * w[j];
           }
           if (lane == 0) {
-            *reinterpret_cast<float4*>(sw + i * COLS + wc) = make_float4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<float4*>(su + i * COLS + wc) = make_float4(u[0], u[1], u[2], u[3]);
+            stw(sw + i * COLS + wc, w);
+            stw(su + i * COLS + wc, u);
           }
         } else {
-          const float4 f = ld4(su + i * COLS + wc);
-          u[0] = f.x;
-          u[1] = f.y;
-          u[2] = f.z;
-          u[3] = f.w;
+          ldw(su + i * COLS + wc, u);
         }
 #pragma unroll
         for (int m = 0; m < RL; ++m) {
@@ -324,11 +382,7 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
           if (i < L) {
             ld_rows<RL>(sla + i * DIN + r0, a);
             ld_rows<RL>(sk + i * DIN + r0, kc);
-            const float4 f = ld4(su + i * COLS + wc);
-            u[0] = f.x;
-            u[1] = f.y;
-            u[2] = f.z;
-            u[3] = f.w;
+            ldw(su + i * COLS + wc, u);
 #pragma unroll
             for (int m = 0; m < RL; ++m) a[m] = __expf(a[m]);
           } else {
@@ -361,9 +415,10 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
         ld_rows<RL>(sk + i * DIN + r0, kc);
         ld_rows<RL>(sla + i * DIN + r0, a);
         const float b = sbeta[i];
-        const float4 d4 = ld4(sdo + i * COLS + wc), u4 = ld4(su + i * COLS + wc),
-                     w4 = ld4(sw + i * COLS + wc);
-        const float dov[CW] = {d4.x, d4.y, d4.z, d4.w}, uv[CW] = {u4.x, u4.y, u4.z, u4.w};
+        float dov[CW], uv[CW], wv[CW];
+        ldw(sdo + i * COLS + wc, dov);
+        ldw(su + i * COLS + wc, uv);
+        ldw(sw + i * COLS + wc, wv);
         // G += scale q do^T, then du = G^T k
         float du[CW];
 #pragma unroll
@@ -379,9 +434,14 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
         }
         warp_sum(du, lane);
         if (lane == 0) {  // dv = beta du, and this block's share of dbeta = du . w
-          *reinterpret_cast<float4*>(p.dv + tok * DIN + vb) =
-              make_float4(b * du[0], b * du[1], b * du[2], b * du[3]);
-          atomicAdd(p.dbeta + tok, du[0] * w4.x + du[1] * w4.y + du[2] * w4.z + du[3] * w4.w);
+          float dvv[CW], db = 0.f;
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            dvv[j] = b * du[j];
+            db += du[j] * wv[j];
+          }
+          stw(p.dv + tok * DIN + vb, dvv);
+          atomicAdd(p.dbeta + tok, db);
         }
         // dq = scale S_t do with S_t = S' + k u^T;  dk = G u - beta S' du;
         // dS' = G - beta k du^T;  dlog_alpha = rowsum(dS' o S')  (this warp's columns)
@@ -416,8 +476,7 @@ __global__ void __launch_bounds__(BwdShape<DIN>::THREADS) kda_bwd_kernel(BwdPara
   if (p.ds0) {
 #pragma unroll
     for (int m = 0; m < RL; ++m)
-      *reinterpret_cast<float4*>(p.ds0 + plane + (size_t)(r0 + m) * DIN + vb) =
-          make_float4(g[m][0], g[m][1], g[m][2], g[m][3]);
+      stw(p.ds0 + plane + (size_t)(r0 + m) * DIN + vb, g[m]);
   }
 }
 
