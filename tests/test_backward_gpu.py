@@ -7,8 +7,9 @@ RMS: several chunks and a ragged tail, a single partial chunk, d = 64 with
 two sequences, no initial state and no final-state gradient, slow decay (the
 gradient carries across every chunk), scale != 1, tokens with beta = 0 (their
 w comes from a column sum, the others' from the forward's u), the empty
-sequence, 80 chains (no u from the forward), and the 8k x 32-head problem
-the bench times (three heads against the oracle).
+sequence, 80 chains (no u from the forward), the 8k x 32-head problem the
+bench times (three heads against the oracle) and the 64k x 32-head problem
+(two heads).
 """
 import numpy as np
 import pytest
@@ -145,4 +146,28 @@ def test_backward_of_the_8k_bench_problem_on_sampled_heads():
         for name in GRADS:
             assert_output_close(got[name][:, :, hs], ref[name], what=f"d{name} head {h}")
         assert_state_close(got["initial_state"][:, hs], ref["initial_state"],
+                           what=f"d initial_state head {h}")
+
+
+def test_backward_of_the_64k_problem_on_sampled_heads():
+    """Training at 64k contexts (the studioglobal.ai page, section "Grosse
+    Kapazitaet..."): the T = 65536, H = 32 problem of the prefill bench
+    (its inputs and seed, random d_out), every head computed on the GPU, two
+    heads (first and last) compared with the oracle in full."""
+    w = gen.WORKLOADS["prefill_64k"]
+    x = gen.workload_inputs(w)
+    r = np.random.default_rng(w.seed + 2)
+    d_out = torch.from_numpy(r.standard_normal((w.B, w.T, w.H, w.dv)).astype(np.float32))
+    g = {k: x[k].cuda() for k in KEYS}
+    got = binding.kda_chunk_bwd(*[g[k] for k in KEYS], d_out.cuda(),
+                                initial_state=x["initial_state"].cuda())
+    torch.cuda.synchronize()
+    assert binding.kda_last_device_status() == 0
+    for h in (0, 31):
+        hs = slice(h, h + 1)
+        ref = orc.kda_recurrence_bwd(*[x[k][:, :, hs] for k in KEYS], x["initial_state"][:, hs],
+                                     d_out[:, :, hs])
+        for name in GRADS:
+            assert_output_close(got[name][:, :, hs].cpu(), ref[name], what=f"d{name} head {h}")
+        assert_state_close(got["initial_state"][:, hs].cpu(), ref["initial_state"],
                            what=f"d initial_state head {h}")
