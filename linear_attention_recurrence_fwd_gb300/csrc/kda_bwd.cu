@@ -25,7 +25,7 @@
 // each group of 4 token states in registers from it.  Lane l holds d_k / 32
 // consecutive rows of G for the warp's columns in registers: dot products
 // along a row stay in the lane, sums down a column (du, and w without u) are
-// a butterfly over the warp.  This is CUDA-core work, serial in tokens per
+// a shuffle reduction over the warp.  This is CUDA-core work, serial in tokens per
 // (sequence, head): an exact token-level formulation, not a tensor-core one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,8 +56,8 @@ struct BwdParams {
 // Work split.  The columns of G evolve independently (each step scales rows
 // and adds rank-one terms), so a warp owns a block of CW value columns for
 // all d_k key rows, lane l the RL = d_k / 32 consecutive rows RL l, ...:
-// a sum down a column (du, and w without u) is then a butterfly over the
-// warp's lanes with no barrier.  Only the gradients summed along a row (dq,
+// a sum down a column (du, and w without u) is then a shuffle reduction over
+// the warp's lanes with no barrier.  Only the gradients summed along a row (dq,
 // dk, dlog_alpha, dbeta) join the column blocks, by atomic adds into zeroed
 // buffers.  A CTA of WPC warps (WPC column blocks of one (sequence, head))
 // stages each chunk's token rows once for all its warps; the warps meet only
